@@ -1,0 +1,222 @@
+/*
+ * spd.h -- sparse paged decode attention for GB300 (sm_103a): the C ABI.
+ *
+ * The library computes the attention hot path of sparse rollouts over a paged
+ * bf16 KV cache: per-page key summaries, query-aware page scoring with a
+ * per-sequence page budget, attention over only the selected pages (split-K
+ * with a log-sum-exp merge), and dense causal verification of k+1 drafted
+ * positions over the whole cache.
+ *
+ * Sources.  Block-sparse (page) attention during rollouts with a KV budget and
+ * a page size, and a Top-k over pages: the Sparrow project page, "Insights" and
+ * "Control Study 2" (cost model; block size 16 and above; page size 16).  A
+ * budget that grows with generation length: Sparrow, "Control Study 1"
+ * (sparsity scheduling).  Sparse drafting of k = 6 tokens and dense
+ * verification over the complete KV cache: the S3R abstract, Figure 6 and
+ * Table 7.  The page score is a Quest-style upper bound from per-page,
+ * per-channel key minima and maxima (Quest is in Sparrow's reference list;
+ * the pages print no scoring rule of their own).
+ *
+ * Conventions shared by every call.
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates, frees or synchronises (except spd_device_status).  Every
+ *    call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *  - bf16 values are passed as raw 16-bit patterns (spd_bf16).  K, V, q, the
+ *    summaries and o must be 16-byte aligned; the KV cache base additionally
+ *    must allow 16-byte row strides (D * 2 bytes, always true for D = 64, 128).
+ *  - Paged KV cache: K and V are [num_phys_pages][H_kv][page_size][D] bf16, so
+ *    one (physical page, KV head) tile is contiguous.  page_table is
+ *    [B][max_pages_per_seq] int32 of physical page ids; seq_lens is [B] int32
+ *    token counts (including the current token, or all T draft tokens).
+ *    Sequence b uses logical pages 0 .. ceil(seq_lens[b] / page_size) - 1; the
+ *    cache slots past seq_lens[b] in its last page are never used for a result
+ *    (their contents may be anything, including NaN).
+ *  - GQA: query head hq reads KV head hq / G, G = H_q / H_kv.
+ *  - Softmax: logits z = softmax_scale * q.k; lse is the natural-log
+ *    log-sum-exp of the scaled logits.  A row that sees no token gets o = 0,
+ *    lse = -inf.
+ *  - Workspace: `ws` is caller-owned device scratch of at least the size the
+ *    matching *_workspace_size function returns.  Its first bytes hold
+ *    counters that MUST be zero before the first call that uses this buffer;
+ *    every successful call leaves them zero again, so a buffer can be reused
+ *    by any later call on the same stream.  Calls that overlap on the GPU must
+ *    use different workspaces.
+ *  - Errors: argument problems are reported synchronously by the returned
+ *    status (nothing is launched); spd_last_error() gives a message.  Problems
+ *    only the GPU can see (a page id outside [0, num_phys_pages), a selection
+ *    entry out of range, a bounded wait that ran out) set bits in a device
+ *    status word read by spd_device_status(); the affected rows are skipped or
+ *    zeroed, and no kernel traps, asserts or spins without a bound.
+ */
+#ifndef SPD_H
+#define SPD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t spd_bf16; /* bfloat16 bit pattern */
+
+typedef enum {
+    SPD_OK = 0,
+    SPD_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, inconsistent shapes */
+    SPD_ERR_UNSUPPORTED = 2, /* a shape outside the supported set (see spd_dims) */
+    SPD_ERR_CUDA = 3,        /* a CUDA runtime or launch error; see spd_last_error() */
+    SPD_ERR_WORKSPACE = 4    /* ws is NULL or ws_bytes is below the required size */
+} spd_status;
+
+/* Device status bits (spd_device_status). */
+#define SPD_DEV_BAD_PAGE 0x1u  /* a page-table entry outside [0, num_phys_pages) */
+#define SPD_DEV_BAD_SEL 0x2u   /* a selected page id outside the sequence, or nsel > k_max */
+#define SPD_DEV_TIMEOUT 0x4u   /* a bounded wait on an asynchronous copy ran out */
+
+/*
+ * Problem shape.  Supported: D in {64, 128}; page_size in {16, 32, 64};
+ * H_kv >= 1, H_q % H_kv == 0, G = H_q / H_kv <= 8; max_pages_per_seq >= 1;
+ * num_phys_pages * H_kv * page_size < 2^31.  B = 0 is a valid no-op.
+ */
+typedef struct {
+    int32_t B;                 /* sequences */
+    int32_t H_q;               /* query heads */
+    int32_t H_kv;              /* KV heads */
+    int32_t D;                 /* head dimension */
+    int32_t page_size;         /* tokens per page */
+    int32_t max_pages_per_seq; /* row length of page_table */
+    int64_t num_phys_pages;    /* pages in the K / V / summary arrays */
+} spd_dims;
+
+typedef enum {
+    SPD_BUDGET_FIXED_PAGES = 0,   /* budget = fixed_pages */
+    SPD_BUDGET_LINEAR_TOKENS = 1, /* ceil(max(min_tokens, ceil(len*slope_num/slope_den) + intercept) / page_size) */
+    SPD_BUDGET_FRACTION = 2       /* ceil(len * frac_num / (frac_den * page_size)) */
+} spd_budget_mode;
+
+/*
+ * Per-sequence page budget (the sparsity schedule), evaluated on the device in
+ * exact 64-bit integer arithmetic from len = seq_lens[b].  The first
+ * sink_pages pages (the attention sink) and the last local_pages pages (the
+ * local window) are always selected and count toward the budget.  The number
+ * of pages selected for a (sequence, KV head) is
+ *   k_eff = min(P, max(min(budget, k_max), |mandatory|)),  P = ceil(len / page_size).
+ */
+typedef struct {
+    int32_t mode; /* spd_budget_mode */
+    int32_t fixed_pages;
+    int64_t min_tokens, slope_num, slope_den, intercept; /* LINEAR_TOKENS (slope_den > 0) */
+    int64_t frac_num, frac_den;                          /* FRACTION (frac_den > 0) */
+    int32_t sink_pages, local_pages;                     /* >= 0 */
+} spd_budget_policy;
+
+/* Library ABI version (major * 100 + minor). */
+int32_t spd_version(void);
+
+/* Message for the last non-OK status returned on this host thread ("" if none). */
+const char *spd_last_error(void);
+
+/*
+ * Reads (and with clear != 0, resets) the device status word of the current
+ * device.  Synchronises the device.  Returns SPD_ERR_CUDA if the read fails.
+ */
+spd_status spd_device_status(uint32_t *out, int32_t clear);
+
+/* Workspace sizes in bytes (0 on invalid arguments; see spd_last_error). */
+size_t spd_score_select_workspace_size(const spd_dims *dims);
+size_t spd_sparse_decode_workspace_size(const spd_dims *dims, int32_t k_max, int32_t num_splits);
+size_t spd_dense_verify_workspace_size(const spd_dims *dims, int32_t T, int32_t num_splits);
+
+/*
+ * pages_summarize -- per-page key summaries (Quest-style page metadata that the
+ * scoring rule reads; the pages' cost model charges one scoring read per
+ * generated page: Sparrow, "Control Study 2", scoring term).
+ *
+ * For each listed page and each KV head h, writes the channel-wise minimum and
+ * maximum of the keys of the page's valid tokens (positions < seq_lens[b]):
+ *   summ[phys][h][0][d] = min_t K[phys][h][t][d],  summ[phys][h][1][d] = max_t ...
+ * summ is bf16 [num_phys_pages][H_kv][2][D]; bf16 min/max is exact.
+ * only_pages: NULL = every logical page of every sequence; otherwise n_only
+ * entries, each b * max_pages_per_seq + p (a slot of page_table), e.g. the
+ * page the newest token was written to.  Entries whose p is past the
+ * sequence's last page are skipped.  Pages not listed are left untouched.
+ */
+spd_status pages_summarize(const spd_dims *dims, const spd_bf16 *K, const int32_t *page_table,
+                           const int32_t *seq_lens, const int32_t *only_pages, int32_t n_only,
+                           spd_bf16 *summ, void *stream);
+
+/*
+ * pages_score_select -- query-aware page scoring plus budgeted top-k
+ * (Sparrow, "Control Study 2": KV budget B, page size, Top-k over pages;
+ * "Control Study 1": length-scheduled budget).
+ *
+ * q is bf16 [B][H_q][D] (the decode query).  For every sequence b, KV head h
+ * and page p < P_b, the score is
+ *   score(p) = max_{g < G} sum_d max(q[b][hG+g][d] * kmin[d], q[b][hG+g][d] * kmax[d])
+ * (an upper bound of q.k over the page's keys), accumulated in fp32 from the
+ * bf16 summaries.  Then the mandatory pages plus the best-scoring remaining
+ * pages (score descending, ties to the lower page id) up to k_eff are
+ * selected and written in ascending page order:
+ *   sel [B][H_kv][k_max] int32 logical page ids (entries past nsel untouched),
+ *   nsel[B][H_kv] int32 = k_eff.
+ * scores: optional fp32 [B][H_kv][max_pages_per_seq] output of the raw scores
+ * (slots past P_b untouched); NULL keeps them in the workspace.
+ * Requires k_max >= sink_pages + local_pages.
+ */
+spd_status pages_score_select(const spd_dims *dims, const spd_bf16 *q, const spd_bf16 *summ,
+                              const int32_t *page_table, const int32_t *seq_lens,
+                              const spd_budget_policy *policy, int32_t *sel, int32_t *nsel,
+                              int32_t k_max, float *scores, void *ws, size_t ws_bytes,
+                              void *stream);
+
+/*
+ * sparse_decode_attn -- attention of the decode query over the selected pages
+ * only (block-sparse page attention: Sparrow, "Insights" and "Control Study
+ * 2"; the S3R sparse drafter of Table 7).
+ *
+ * For each sequence b and query head hq (KV head h = hq / G): exact softmax
+ * attention over the valid tokens of pages sel[b][h][0 .. nsel[b][h]):
+ *   o[b][hq][d] (bf16), lse[b][hq] (fp32, natural log; may be NULL).
+ * num_splits: 0 = automatic; otherwise the selected list of each (b, h) is cut
+ * into that many contiguous parts processed in parallel and merged with the
+ * log-sum-exp rule of lse_merge.  The workspace must hold
+ * spd_sparse_decode_workspace_size(dims, k_max, num_splits) bytes.
+ */
+spd_status sparse_decode_attn(const spd_dims *dims, const spd_bf16 *q, const spd_bf16 *K,
+                              const spd_bf16 *V, const int32_t *page_table,
+                              const int32_t *seq_lens, const int32_t *sel, const int32_t *nsel,
+                              int32_t k_max, int32_t num_splits, float softmax_scale,
+                              spd_bf16 *o, float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * dense_verify_attn -- dense causal verification of T drafted positions over
+ * the complete KV cache (S3R abstract; Table 7 "Verify (TV)", k = 6 so T = 7).
+ *
+ * q is bf16 [B][T][H_q][D]; the drafted tokens' K/V are already the last T
+ * tokens of each sequence.  Row t (absolute position seq_lens[b] - T + t)
+ * attends over tokens 0 .. seq_lens[b] - T + t.  Outputs o bf16 [B][T][H_q][D]
+ * and lse fp32 [B][T][H_q] (may be NULL).  T = 1 is dense decode attention.
+ * Supported: 1 <= T and T * G <= 64.  num_splits: 0 = automatic.
+ */
+spd_status dense_verify_attn(const spd_dims *dims, int32_t T, const spd_bf16 *q,
+                             const spd_bf16 *K, const spd_bf16 *V, const int32_t *page_table,
+                             const int32_t *seq_lens, int32_t num_splits, float softmax_scale,
+                             spd_bf16 *o, float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * lse_merge -- combine S partial attention results computed over disjoint
+ * token sets (split-K FlashDecoding):
+ *   lse = log sum_s exp(part_lse[s]),  o = sum_s exp(part_lse[s] - lse) * part_o[s].
+ * part_o fp32 [S][rows][D] (each partial already normalised), part_lse fp32
+ * [S][rows] (natural log; -inf marks an empty partial).  Writes o bf16
+ * [rows][D] and lse fp32 [rows] (lse may be NULL).  All partials empty:
+ * o = 0, lse = -inf.  Supported: S >= 1, D in {64, 128}.
+ */
+spd_status lse_merge(int32_t S, int32_t rows, int32_t D, const float *part_o,
+                     const float *part_lse, spd_bf16 *o, float *lse, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPD_H */

@@ -1,0 +1,189 @@
+"""Sparse paged decode attention for GB300: a thin Python binding over ``libspd.so``.
+
+The functions here carry the names of the C ABI (``include/spd.h``) and only
+marshal arguments: every step runs in the library's CUDA kernels.  PyTorch
+supplies device memory and the current stream.  There is no fallback: if the
+library is missing or a call fails, a ``SpdError`` is raised.
+
+Tensors: bf16 data may be ``torch.bfloat16`` or ``torch.uint16`` (same bits);
+index data is ``torch.int32``; everything contiguous and on the current device.
+Workspaces are zero-initialised byte tensors (see ``workspace``); each call
+leaves its counters at zero, so a workspace can be reused on one stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+__all__ = [
+    "SpdError", "Dims", "Policy", "lib", "dims_of", "policy_of", "workspace",
+    "pages_summarize", "pages_score_select", "sparse_decode_attn", "dense_verify_attn",
+    "lse_merge", "spd_device_status", "spd_score_select_workspace_size",
+    "spd_sparse_decode_workspace_size", "spd_dense_verify_workspace_size",
+    "DEV_BAD_PAGE", "DEV_BAD_SEL", "DEV_TIMEOUT",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspd.so")
+
+DEV_BAD_PAGE, DEV_BAD_SEL, DEV_TIMEOUT = 0x1, 0x2, 0x4
+_STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "WORKSPACE"}
+_MODES = {"fixed": 0, "linear": 1, "fraction": 2}
+
+
+class SpdError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"spd {_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H_q", ctypes.c_int32), ("H_kv", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("max_pages_per_seq", ctypes.c_int32), ("num_phys_pages", ctypes.c_int64)]
+
+
+class Policy(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("fixed_pages", ctypes.c_int32),
+                ("min_tokens", ctypes.c_int64), ("slope_num", ctypes.c_int64),
+                ("slope_den", ctypes.c_int64), ("intercept", ctypes.c_int64),
+                ("frac_num", ctypes.c_int64), ("frac_den", ctypes.c_int64),
+                ("sink_pages", ctypes.c_int32), ("local_pages", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libspd.so (fails loudly when it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise SpdError(3, f"{LIB_PATH} is missing: build it with "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        DP, PP = ctypes.POINTER(Dims), ctypes.POINTER(Policy)
+        L.spd_version.restype = i32
+        L.spd_last_error.restype = ctypes.c_char_p
+        L.spd_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+        L.spd_score_select_workspace_size.argtypes = [DP]
+        L.spd_score_select_workspace_size.restype = sz
+        L.spd_sparse_decode_workspace_size.argtypes = [DP, i32, i32]
+        L.spd_sparse_decode_workspace_size.restype = sz
+        L.spd_dense_verify_workspace_size.argtypes = [DP, i32, i32]
+        L.spd_dense_verify_workspace_size.restype = sz
+        L.pages_summarize.argtypes = [DP, P, P, P, P, i32, P, P]
+        L.pages_score_select.argtypes = [DP, P, P, P, P, PP, P, P, i32, P, P, sz, P]
+        L.sparse_decode_attn.argtypes = [DP, P, P, P, P, P, P, P, i32, i32, ctypes.c_float,
+                                         P, P, P, sz, P]
+        L.dense_verify_attn.argtypes = [DP, i32, P, P, P, P, P, i32, ctypes.c_float, P, P, P, sz, P]
+        L.lse_merge.argtypes = [i32, i32, i32, P, P, P, P, P]
+        for f in ("spd_device_status", "pages_summarize", "pages_score_select",
+                  "sparse_decode_attn", "dense_verify_attn", "lse_merge"):
+            getattr(L, f).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise SpdError(status, lib().spd_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise SpdError(1, "tensor is not on a CUDA device")
+    if not t.is_contiguous():
+        raise SpdError(1, "tensor is not contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def dims_of(B, H_q, H_kv, D, page_size, max_pages_per_seq, num_phys_pages) -> Dims:
+    return Dims(B, H_q, H_kv, D, page_size, max_pages_per_seq, num_phys_pages)
+
+
+def policy_of(p) -> Policy:
+    """A ``Policy`` from any object with the fields of ``workloads.BudgetPolicy``."""
+    return Policy(_MODES[p.mode] if isinstance(p.mode, str) else int(p.mode), p.fixed_pages,
+                  p.min_tokens, p.slope_num, p.slope_den, p.intercept, p.frac_num, p.frac_den,
+                  p.sink_pages, p.local_pages)
+
+
+def _size(v: int, what: str) -> int:
+    if v == 0:
+        raise SpdError(1, f"{what}: " + lib().spd_last_error().decode(errors="replace"))
+    return v
+
+
+def spd_score_select_workspace_size(dims: Dims) -> int:
+    return _size(lib().spd_score_select_workspace_size(ctypes.byref(dims)), "score_select workspace")
+
+
+def spd_sparse_decode_workspace_size(dims: Dims, k_max: int, num_splits: int = 0) -> int:
+    return _size(lib().spd_sparse_decode_workspace_size(ctypes.byref(dims), k_max, num_splits),
+                 "sparse_decode workspace")
+
+
+def spd_dense_verify_workspace_size(dims: Dims, T: int, num_splits: int = 0) -> int:
+    return _size(lib().spd_dense_verify_workspace_size(ctypes.byref(dims), T, num_splits),
+                 "dense_verify workspace")
+
+
+def workspace(nbytes: int, device=None):
+    """A zeroed byte tensor usable as a workspace (allocated by PyTorch, not the library)."""
+    import torch
+    return torch.zeros(max(1, int(nbytes)), dtype=torch.uint8, device=device or "cuda")
+
+
+def spd_device_status(clear: bool = False) -> int:
+    v = ctypes.c_uint32(0)
+    _check(lib().spd_device_status(ctypes.byref(v), 1 if clear else 0))
+    return v.value
+
+
+def pages_summarize(dims: Dims, K, page_table, seq_lens, summ, only_pages=None, stream=None):
+    n_only = 0 if only_pages is None else only_pages.numel()
+    _check(lib().pages_summarize(ctypes.byref(dims), _ptr(K), _ptr(page_table), _ptr(seq_lens),
+                                 _ptr(only_pages), n_only, _ptr(summ), _stream(stream)))
+
+
+def pages_score_select(dims: Dims, q, summ, page_table, seq_lens, policy, sel, nsel, k_max: int,
+                       ws, scores=None, stream=None):
+    pol = policy if isinstance(policy, Policy) else policy_of(policy)
+    _check(lib().pages_score_select(ctypes.byref(dims), _ptr(q), _ptr(summ), _ptr(page_table),
+                                    _ptr(seq_lens), ctypes.byref(pol), _ptr(sel), _ptr(nsel), k_max,
+                                    _ptr(scores), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def sparse_decode_attn(dims: Dims, q, K, V, page_table, seq_lens, sel, nsel, k_max: int, o, ws,
+                       lse=None, num_splits: int = 0, softmax_scale: float | None = None,
+                       stream=None):
+    scale = 1.0 / math.sqrt(dims.D) if softmax_scale is None else softmax_scale
+    _check(lib().sparse_decode_attn(ctypes.byref(dims), _ptr(q), _ptr(K), _ptr(V), _ptr(page_table),
+                                    _ptr(seq_lens), _ptr(sel), _ptr(nsel), k_max, num_splits,
+                                    scale, _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
+                                    _stream(stream)))
+
+
+def dense_verify_attn(dims: Dims, T: int, q, K, V, page_table, seq_lens, o, ws, lse=None,
+                      num_splits: int = 0, softmax_scale: float | None = None, stream=None):
+    scale = 1.0 / math.sqrt(dims.D) if softmax_scale is None else softmax_scale
+    _check(lib().dense_verify_attn(ctypes.byref(dims), T, _ptr(q), _ptr(K), _ptr(V),
+                                   _ptr(page_table), _ptr(seq_lens), num_splits, scale, _ptr(o),
+                                   _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def lse_merge(part_o, part_lse, o, lse=None, stream=None):
+    S, rows, D = part_o.shape
+    _check(lib().lse_merge(S, rows, D, _ptr(part_o), _ptr(part_lse), _ptr(o), _ptr(lse),
+                           _stream(stream)))

@@ -1,0 +1,80 @@
+// kernels.h -- host-side launch interface between the C-ABI layer (spd_api.cu)
+// and the kernel translation units.  Internal to the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/spd.h"
+
+namespace spd {
+
+struct SummarizeArgs {
+    const uint16_t* K;
+    const int32_t* page_table;
+    const int32_t* seq_lens;
+    const int32_t* only_pages;  // NULL = all pages
+    int n_only;
+    uint16_t* summ;
+    int B, H_kv, D, ps, max_pages;
+    long long num_phys;
+    unsigned* status;
+};
+cudaError_t launch_summarize(const SummarizeArgs& a, cudaStream_t st);
+
+struct ScoreSelectArgs {
+    const uint16_t* q;
+    const uint16_t* summ;
+    const int32_t* page_table;
+    const int32_t* seq_lens;
+    spd_budget_policy pol;
+    int32_t* sel;
+    int32_t* nsel;
+    int k_max;
+    float* scores;    // [B][H_kv][max_pages]
+    int* counters;    // [B][H_kv], zero on entry and on exit
+    int B, H_q, H_kv, D, ps, max_pages;
+    long long num_phys;
+    unsigned* status;
+};
+// Pages scored per CTA (a multiple of 64), and the dynamic shared memory the
+// selection needs.
+int score_chunk_pages(int max_pages, int rows, int num_sms);
+cudaError_t launch_score_select(const ScoreSelectArgs& a, int chunk_pages, cudaStream_t st);
+
+struct AttnArgs {
+    const uint16_t* q;  // [B][T][H_q][D] (T = 1 for decode)
+    const int32_t* page_table;
+    const int32_t* seq_lens;
+    const int32_t* sel;   // sparse only
+    const int32_t* nsel;  // sparse only
+    int k_max;
+    int B, H_q, H_kv, D, ps, max_pages, T;
+    long long num_phys;
+    int items_per_split, num_splits;
+    float scale_log2;
+    uint16_t* o;
+    float* lse;
+    float* part_o;
+    float* part_lse;
+    int* counters;
+    unsigned* status;
+};
+// Rows (T * G) handled per CTA, padded to 16-row MMA tiles.
+inline int attn_mtiles(int T, int G) {
+    int r = T * G;
+    return r <= 16 ? 1 : (r <= 32 ? 2 : 4);
+}
+cudaError_t launch_sparse_attn(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                               cudaStream_t st);
+cudaError_t launch_dense_attn(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                              cudaStream_t st);
+// CTAs of the attention kernel that fit on one SM for this shape.
+int occ_sparse_attn(int D, int ps);
+int occ_dense_attn(int D, int ps, int mtiles);
+
+cudaError_t launch_lse_merge(int S, int rows, int D, const float* part_o, const float* part_lse,
+                             uint16_t* o, float* lse, cudaStream_t st);
+
+}  // namespace spd

@@ -1,0 +1,437 @@
+// spd_api.cu -- the C ABI of libspd (declared in include/spd.h): argument
+// validation, workspace carving, TMA tensor-map encoding, launch-shape choice
+// and dispatch to the kernels.  Nothing here allocates device memory or
+// synchronises (except spd_device_status).
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "kernels.h"
+
+#define SPD_API extern "C" __attribute__((visibility("default")))
+
+namespace spd {
+namespace {
+
+thread_local std::string g_err;
+
+// Device status word (SPD_DEV_* bits), one per device that loads the library.
+__device__ unsigned g_status;
+
+spd_status fail(spd_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return s;
+}
+
+spd_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(SPD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DevInfo {
+    std::once_flag once;
+    unsigned* status = nullptr;
+    int sms = 0;
+    cudaError_t err = cudaSuccess;
+};
+DevInfo g_dev[kMaxDevices];
+
+DevInfo* dev_info(spd_status* st) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *st = cuda_fail(e, "cudaGetDevice");
+        return nullptr;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        *st = fail(SPD_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+        return nullptr;
+    }
+    DevInfo* d = &g_dev[dev];
+    std::call_once(d->once, [d, dev]() {
+        void* p = nullptr;
+        d->err = cudaGetSymbolAddress(&p, g_status);
+        if (d->err == cudaSuccess) d->status = static_cast<unsigned*>(p);
+        if (d->err == cudaSuccess) d->err = cudaDeviceGetAttribute(&d->sms, cudaDevAttrMultiProcessorCount, dev);
+    });
+    if (d->err != cudaSuccess) {
+        *st = cuda_fail(d->err, "device set-up");
+        return nullptr;
+    }
+    return d;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn(spd_status* st) {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    if (!fn) *st = fail(SPD_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable (%s)", cudaGetErrorString(err));
+    return fn;
+}
+
+// 2-D view of a paged K or V cache: rows = num_phys * H_kv * ps, D bf16 each;
+// box = ps rows x 64 elements (128 bytes), 128-byte swizzle.
+spd_status kv_map(CUtensorMap* m, const void* base, const spd_dims* d) {
+    spd_status st = SPD_OK;
+    EncodeTiledFn fn = encode_fn(&st);
+    if (!fn) return st;
+    cuuint64_t gdim[2] = {(cuuint64_t)d->D, (cuuint64_t)d->num_phys_pages * d->H_kv * d->page_size};
+    cuuint64_t gstride[1] = {(cuuint64_t)d->D * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)d->page_size};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(SPD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return SPD_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+spd_status check_dims(const spd_dims* d) {
+    if (!d) return fail(SPD_ERR_INVALID_ARG, "dims is NULL");
+    if (d->B < 0 || d->H_q <= 0 || d->H_kv <= 0 || d->max_pages_per_seq <= 0 || d->num_phys_pages < 0)
+        return fail(SPD_ERR_INVALID_ARG, "bad dims (B=%d H_q=%d H_kv=%d max_pages=%d num_phys=%lld)", d->B,
+                    d->H_q, d->H_kv, d->max_pages_per_seq, (long long)d->num_phys_pages);
+    if (d->H_q % d->H_kv) return fail(SPD_ERR_INVALID_ARG, "H_q (%d) is not a multiple of H_kv (%d)", d->H_q, d->H_kv);
+    if (d->H_q / d->H_kv > 8) return fail(SPD_ERR_UNSUPPORTED, "GQA group %d > 8", d->H_q / d->H_kv);
+    if (d->D != 64 && d->D != 128) return fail(SPD_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", d->D);
+    if (d->page_size != 16 && d->page_size != 32 && d->page_size != 64)
+        return fail(SPD_ERR_UNSUPPORTED, "page size %d (supported: 16, 32, 64)", d->page_size);
+    if ((long long)d->num_phys_pages * d->H_kv * d->page_size >= (1LL << 31))
+        return fail(SPD_ERR_UNSUPPORTED, "num_phys_pages * H_kv * page_size must be < 2^31");
+    if ((long long)d->B * d->max_pages_per_seq >= (1LL << 31))
+        return fail(SPD_ERR_UNSUPPORTED, "B * max_pages_per_seq must be < 2^31");
+    return SPD_OK;
+}
+
+int pages_per_split_floor(int ps) { return ps >= 64 ? 2 : (ps == 32 ? 4 : 8); }
+
+// Splits of a selected-page list: enough CTAs for ~2 waves of the GPU, with at
+// least a few pages per split.
+int sparse_splits(const spd_dims* d, int k_max, int req, int sms) {
+    int S = req;
+    if (S <= 0) {
+        const long long rows = (long long)d->B * d->H_kv;
+        const long long slots = (long long)sms * occ_sparse_attn(d->D, d->page_size);
+        const int floor_items = pages_per_split_floor(d->page_size);
+        S = 1;
+        while (rows * S < 2 * slots && (k_max + 2 * S - 1) / (2 * S) >= floor_items) S *= 2;
+    }
+    if (S > k_max) S = k_max;
+    if (S < 1) S = 1;
+    const int ips = (k_max + S - 1) / S;
+    return (k_max + ips - 1) / ips;
+}
+
+int dense_splits(const spd_dims* d, int T, int req, int sms) {
+    const int P = d->max_pages_per_seq;
+    int S = req;
+    if (S <= 0) {
+        const long long rows = (long long)d->B * d->H_kv;
+        const int mt = attn_mtiles(T, d->H_q / d->H_kv);
+        const long long slots = (long long)sms * occ_dense_attn(d->D, d->page_size, mt);
+        const int floor_items = 2 * pages_per_split_floor(d->page_size);
+        S = 1;
+        while (rows * S < 4 * slots && (P + 2 * S - 1) / (2 * S) >= floor_items) S *= 2;
+    }
+    if (S > P) S = P;
+    if (S < 1) S = 1;
+    const int ips = (P + S - 1) / S;
+    return (P + ips - 1) / ips;
+}
+
+struct AttnWs {
+    int* counters;
+    float* part_lse;
+    float* part_o;
+    size_t bytes;
+};
+
+AttnWs attn_ws_layout(void* ws, long long rows, int S, int R, int D) {
+    AttnWs w;
+    size_t off = 0;
+    w.counters = reinterpret_cast<int*>(ws);
+    off += align256(rows * sizeof(int));
+    w.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + off);
+    off += align256((size_t)rows * S * R * sizeof(float));
+    w.part_o = reinterpret_cast<float*>(static_cast<char*>(ws) + off);
+    off += (size_t)rows * S * R * D * sizeof(float);
+    w.bytes = off;
+    return w;
+}
+
+}  // namespace
+}  // namespace spd
+
+using namespace spd;
+
+SPD_API int32_t spd_version(void) { return 100; }
+
+SPD_API const char* spd_last_error(void) { return g_err.c_str(); }
+
+SPD_API spd_status spd_device_status(uint32_t* out, int32_t clear) {
+    if (!out) return fail(SPD_ERR_INVALID_ARG, "out is NULL");
+    spd_status st = SPD_OK;
+    DevInfo* d = dev_info(&st);
+    if (!d) return st;
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpy(&v, d->status, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
+    *out = v;
+    if (clear) {
+        e = cudaMemset(d->status, 0, sizeof(unsigned));
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the device status");
+    }
+    return SPD_OK;
+}
+
+SPD_API size_t spd_score_select_workspace_size(const spd_dims* dims) {
+    if (check_dims(dims) != SPD_OK) return 0;
+    const long long rows = (long long)dims->B * dims->H_kv;
+    return align256(rows * sizeof(int)) + (size_t)rows * dims->max_pages_per_seq * sizeof(float);
+}
+
+SPD_API size_t spd_sparse_decode_workspace_size(const spd_dims* dims, int32_t k_max, int32_t num_splits) {
+    if (check_dims(dims) != SPD_OK) return 0;
+    if (k_max < 1) {
+        fail(SPD_ERR_INVALID_ARG, "k_max < 1");
+        return 0;
+    }
+    spd_status st = SPD_OK;
+    DevInfo* d = dev_info(&st);
+    if (!d) return 0;
+    const int S = sparse_splits(dims, k_max, num_splits, d->sms);
+    return attn_ws_layout(nullptr, (long long)dims->B * dims->H_kv, S, dims->H_q / dims->H_kv, dims->D).bytes;
+}
+
+SPD_API size_t spd_dense_verify_workspace_size(const spd_dims* dims, int32_t T, int32_t num_splits) {
+    if (check_dims(dims) != SPD_OK) return 0;
+    if (T < 1 || T * (dims->H_q / dims->H_kv) > 64) {
+        fail(SPD_ERR_UNSUPPORTED, "T=%d with G=%d (need 1 <= T and T*G <= 64)", T, dims->H_q / dims->H_kv);
+        return 0;
+    }
+    spd_status st = SPD_OK;
+    DevInfo* d = dev_info(&st);
+    if (!d) return 0;
+    const int S = dense_splits(dims, T, num_splits, d->sms);
+    return attn_ws_layout(nullptr, (long long)dims->B * dims->H_kv, S, T * (dims->H_q / dims->H_kv), dims->D).bytes;
+}
+
+SPD_API spd_status pages_summarize(const spd_dims* dims, const spd_bf16* K, const int32_t* page_table,
+                                   const int32_t* seq_lens, const int32_t* only_pages, int32_t n_only,
+                                   spd_bf16* summ, void* stream) {
+    spd_status st = check_dims(dims);
+    if (st != SPD_OK) return st;
+    if (dims->B == 0 || (only_pages && n_only == 0)) return SPD_OK;
+    if (!K || !page_table || !seq_lens || !summ) return fail(SPD_ERR_INVALID_ARG, "NULL pointer argument");
+    if (only_pages && n_only < 0) return fail(SPD_ERR_INVALID_ARG, "n_only < 0");
+    if (!aligned16(K) || !aligned16(summ)) return fail(SPD_ERR_INVALID_ARG, "K and summ must be 16-byte aligned");
+    DevInfo* d = dev_info(&st);
+    if (!d) return st;
+    SummarizeArgs a;
+    a.K = K;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.only_pages = only_pages;
+    a.n_only = n_only;
+    a.summ = summ;
+    a.B = dims->B;
+    a.H_kv = dims->H_kv;
+    a.D = dims->D;
+    a.ps = dims->page_size;
+    a.max_pages = dims->max_pages_per_seq;
+    a.num_phys = dims->num_phys_pages;
+    a.status = d->status;
+    cudaError_t e = launch_summarize(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPD_OK : cuda_fail(e, "pages_summarize launch");
+}
+
+SPD_API spd_status pages_score_select(const spd_dims* dims, const spd_bf16* q, const spd_bf16* summ,
+                                      const int32_t* page_table, const int32_t* seq_lens,
+                                      const spd_budget_policy* policy, int32_t* sel, int32_t* nsel, int32_t k_max,
+                                      float* scores, void* ws, size_t ws_bytes, void* stream) {
+    spd_status st = check_dims(dims);
+    if (st != SPD_OK) return st;
+    if (!policy) return fail(SPD_ERR_INVALID_ARG, "policy is NULL");
+    const spd_budget_policy& p = *policy;
+    if (p.mode < 0 || p.mode > 2) return fail(SPD_ERR_INVALID_ARG, "unknown budget mode %d", p.mode);
+    if (p.sink_pages < 0 || p.local_pages < 0) return fail(SPD_ERR_INVALID_ARG, "negative sink/local pages");
+    if (p.mode == SPD_BUDGET_FIXED_PAGES && p.fixed_pages < 0) return fail(SPD_ERR_INVALID_ARG, "fixed_pages < 0");
+    if (p.mode == SPD_BUDGET_LINEAR_TOKENS && (p.slope_den <= 0 || p.slope_num < 0 || p.min_tokens < 0))
+        return fail(SPD_ERR_INVALID_ARG, "bad linear budget parameters");
+    if (p.mode == SPD_BUDGET_FRACTION && (p.frac_den <= 0 || p.frac_num < 0))
+        return fail(SPD_ERR_INVALID_ARG, "bad fraction budget parameters");
+    if (k_max < 1 || (long long)k_max < (long long)p.sink_pages + p.local_pages)
+        return fail(SPD_ERR_INVALID_ARG, "k_max (%d) must be >= 1 and >= sink_pages + local_pages", k_max);
+    if (dims->max_pages_per_seq > 32768)
+        return fail(SPD_ERR_UNSUPPORTED, "max_pages_per_seq %d > 32768", dims->max_pages_per_seq);
+    if (dims->B == 0) return SPD_OK;
+    if (!q || !summ || !page_table || !seq_lens || !sel || !nsel)
+        return fail(SPD_ERR_INVALID_ARG, "NULL pointer argument");
+    if (!aligned16(q) || !aligned16(summ)) return fail(SPD_ERR_INVALID_ARG, "q and summ must be 16-byte aligned");
+    const size_t need = spd_score_select_workspace_size(dims);
+    if (!ws || ws_bytes < need) return fail(SPD_ERR_WORKSPACE, "workspace %zu bytes < %zu", ws_bytes, need);
+    DevInfo* d = dev_info(&st);
+    if (!d) return st;
+    const long long rows = (long long)dims->B * dims->H_kv;
+    ScoreSelectArgs a;
+    a.q = q;
+    a.summ = summ;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.pol = p;
+    a.sel = sel;
+    a.nsel = nsel;
+    a.k_max = k_max;
+    a.counters = static_cast<int*>(ws);
+    a.scores = scores ? scores : reinterpret_cast<float*>(static_cast<char*>(ws) + align256(rows * sizeof(int)));
+    a.B = dims->B;
+    a.H_q = dims->H_q;
+    a.H_kv = dims->H_kv;
+    a.D = dims->D;
+    a.ps = dims->page_size;
+    a.max_pages = dims->max_pages_per_seq;
+    a.num_phys = dims->num_phys_pages;
+    a.status = d->status;
+    const int cp = score_chunk_pages(a.max_pages, (int)rows, d->sms);
+    cudaError_t e = launch_score_select(a, cp, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPD_OK : cuda_fail(e, "pages_score_select launch");
+}
+
+static spd_status attn_common(const spd_dims* dims, const spd_bf16* q, const spd_bf16* K, const spd_bf16* V,
+                              const int32_t* page_table, const int32_t* seq_lens, spd_bf16* o) {
+    if (!q || !K || !V || !page_table || !seq_lens || !o) return fail(SPD_ERR_INVALID_ARG, "NULL pointer argument");
+    if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(o))
+        return fail(SPD_ERR_INVALID_ARG, "q, K, V and o must be 16-byte aligned");
+    if (dims->num_phys_pages < 1) return fail(SPD_ERR_INVALID_ARG, "num_phys_pages < 1");
+    return SPD_OK;
+}
+
+SPD_API spd_status sparse_decode_attn(const spd_dims* dims, const spd_bf16* q, const spd_bf16* K,
+                                      const spd_bf16* V, const int32_t* page_table, const int32_t* seq_lens,
+                                      const int32_t* sel, const int32_t* nsel, int32_t k_max, int32_t num_splits,
+                                      float softmax_scale, spd_bf16* o, float* lse, void* ws, size_t ws_bytes,
+                                      void* stream) {
+    spd_status st = check_dims(dims);
+    if (st != SPD_OK) return st;
+    if (k_max < 1) return fail(SPD_ERR_INVALID_ARG, "k_max < 1");
+    if (num_splits < 0) return fail(SPD_ERR_INVALID_ARG, "num_splits < 0");
+    if (dims->B == 0) return SPD_OK;
+    if ((st = attn_common(dims, q, K, V, page_table, seq_lens, o)) != SPD_OK) return st;
+    if (!sel || !nsel) return fail(SPD_ERR_INVALID_ARG, "NULL selection");
+    DevInfo* d = dev_info(&st);
+    if (!d) return st;
+    const int S = sparse_splits(dims, k_max, num_splits, d->sms);
+    const int G = dims->H_q / dims->H_kv;
+    const long long rows = (long long)dims->B * dims->H_kv;
+    AttnWs w = attn_ws_layout(ws, rows, S, G, dims->D);
+    if (!ws || ws_bytes < w.bytes) return fail(SPD_ERR_WORKSPACE, "workspace %zu bytes < %zu", ws_bytes, w.bytes);
+    CUtensorMap tk, tv;
+    if ((st = kv_map(&tk, K, dims)) != SPD_OK || (st = kv_map(&tv, V, dims)) != SPD_OK) return st;
+    AttnArgs a;
+    a.q = q;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.sel = sel;
+    a.nsel = nsel;
+    a.k_max = k_max;
+    a.B = dims->B;
+    a.H_q = dims->H_q;
+    a.H_kv = dims->H_kv;
+    a.D = dims->D;
+    a.ps = dims->page_size;
+    a.max_pages = dims->max_pages_per_seq;
+    a.T = 1;
+    a.num_phys = dims->num_phys_pages;
+    a.items_per_split = (k_max + S - 1) / S;
+    a.num_splits = S;
+    a.scale_log2 = softmax_scale * kLog2e;
+    a.o = o;
+    a.lse = lse;
+    a.part_o = w.part_o;
+    a.part_lse = w.part_lse;
+    a.counters = w.counters;
+    a.status = d->status;
+    cudaError_t e = launch_sparse_attn(a, tk, tv, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPD_OK : cuda_fail(e, "sparse_decode_attn launch");
+}
+
+SPD_API spd_status dense_verify_attn(const spd_dims* dims, int32_t T, const spd_bf16* q, const spd_bf16* K,
+                                     const spd_bf16* V, const int32_t* page_table, const int32_t* seq_lens,
+                                     int32_t num_splits, float softmax_scale, spd_bf16* o, float* lse, void* ws,
+                                     size_t ws_bytes, void* stream) {
+    spd_status st = check_dims(dims);
+    if (st != SPD_OK) return st;
+    const int G = dims->H_q / dims->H_kv;
+    if (T < 1 || T * G > 64) return fail(SPD_ERR_UNSUPPORTED, "T=%d with G=%d (need 1 <= T and T*G <= 64)", T, G);
+    if (num_splits < 0) return fail(SPD_ERR_INVALID_ARG, "num_splits < 0");
+    if (dims->B == 0) return SPD_OK;
+    if ((st = attn_common(dims, q, K, V, page_table, seq_lens, o)) != SPD_OK) return st;
+    DevInfo* d = dev_info(&st);
+    if (!d) return st;
+    const int S = dense_splits(dims, T, num_splits, d->sms);
+    const long long rows = (long long)dims->B * dims->H_kv;
+    AttnWs w = attn_ws_layout(ws, rows, S, T * G, dims->D);
+    if (!ws || ws_bytes < w.bytes) return fail(SPD_ERR_WORKSPACE, "workspace %zu bytes < %zu", ws_bytes, w.bytes);
+    CUtensorMap tk, tv;
+    if ((st = kv_map(&tk, K, dims)) != SPD_OK || (st = kv_map(&tv, V, dims)) != SPD_OK) return st;
+    AttnArgs a;
+    a.q = q;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.sel = nullptr;
+    a.nsel = nullptr;
+    a.k_max = 0;
+    a.B = dims->B;
+    a.H_q = dims->H_q;
+    a.H_kv = dims->H_kv;
+    a.D = dims->D;
+    a.ps = dims->page_size;
+    a.max_pages = dims->max_pages_per_seq;
+    a.T = T;
+    a.num_phys = dims->num_phys_pages;
+    a.items_per_split = (dims->max_pages_per_seq + S - 1) / S;
+    a.num_splits = S;
+    a.scale_log2 = softmax_scale * kLog2e;
+    a.o = o;
+    a.lse = lse;
+    a.part_o = w.part_o;
+    a.part_lse = w.part_lse;
+    a.counters = w.counters;
+    a.status = d->status;
+    cudaError_t e = launch_dense_attn(a, tk, tv, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPD_OK : cuda_fail(e, "dense_verify_attn launch");
+}
+
+SPD_API spd_status lse_merge(int32_t S, int32_t rows, int32_t D, const float* part_o, const float* part_lse,
+                             spd_bf16* o, float* lse, void* stream) {
+    if (S < 1 || rows < 0) return fail(SPD_ERR_INVALID_ARG, "bad S (%d) or rows (%d)", S, rows);
+    if (D != 64 && D != 128) return fail(SPD_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", D);
+    if (rows == 0) return SPD_OK;
+    if (!part_o || !part_lse || !o) return fail(SPD_ERR_INVALID_ARG, "NULL pointer argument");
+    cudaError_t e = launch_lse_merge(S, rows, D, part_o, part_lse, o, lse, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPD_OK : cuda_fail(e, "lse_merge launch");
+}

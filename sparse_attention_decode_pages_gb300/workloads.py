@@ -294,3 +294,20 @@ def make(s: Spec, threads: int | None = None) -> Workload:
 
 def named(name: str, page_size: int | None = None, threads: int | None = None, **over) -> Workload:
     return make(spec(name, page_size, **over), threads)
+
+
+def to_device(w: Workload, device="cuda") -> dict:
+    """Copy a workload's arrays to the GPU as torch tensors (bf16 data keeps its bit patterns)."""
+    import torch
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).to(device)
+
+    out = dict(
+        q=bf(w.q), K=bf(w.K), V=bf(w.V),
+        page_table=torch.from_numpy(w.page_table).to(device),
+        seq_lens=torch.from_numpy(w.seq_lens).to(device),
+    )
+    if w.q_verify is not None:
+        out["q_verify"] = bf(w.q_verify)
+    return out
