@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Benchmark: sparse paged decode attention on the Qwen3-8B-shaped workload.
+
+One step is one pass of the hot path over one batch (B = 64 sequences, 32 query
+/ 8 KV heads, head dim 128, contexts 8K..16K, page size 16, budget 64 pages):
+
+  a1  summary refresh of the page each sequence's newest token landed in
+      (pages_summarize on B listed pages),
+  a2-a4  pages_score_select (upper-bound scores of every page, top-k budget),
+  a5-a6  sparse_decode_attn (split-K over the selected pages, fused merge),
+  a7  dense_verify_attn of k+1 = 7 drafted positions over the full cache.
+
+The headline metric is sparse decode-attention tokens/s (B tokens per pass of
+a1-a6); a7 is timed in the same steps and reported under "dense_verify".  Each
+kernel is timed with CUDA events on the launching stream; L2 is flushed (a
+256 MiB write) between timed passes, outside the events.  The KV cache and the
+page summaries are resident in HBM (they are the cache); e2e adds, per step,
+the host->device copy of the step's inputs (q, seq_lens, page_table) from
+pinned memory and the device->host copy of o and lse.
+
+--impl reference times the fp64 CPU oracle (there is no other reference
+implementation of this path) on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_attention_decode_pages_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "sparse decode-attn tokens/s and HBM GB/s (% of roofline), Qwen3-8B shape"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = ["common.cuh", "attn.cuh", "attn_sparse.cu", "score_select.cu", "summarize.cu"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "sparse_attention_decode_pages_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(w, nsel):
+    """Bytes the method must move per pass (valid tokens of selected pages, summaries, q/o/lse)."""
+    ps, D, H_kv = w.page_size, w.D, w.H_kv
+    kv = 0
+    summ = 0
+    for b in range(w.B):
+        L = int(w.seq_lens[b])
+        P = w.pages(b)
+        summ += P * H_kv * 4 * D
+        for h in range(H_kv):
+            pages = nsel[b][h]
+            toks = sum(min(ps, L - p * ps) for p in pages)
+            kv += toks * 4 * D
+    qo = w.B * w.H_q * D * 2 * 2 + w.B * w.H_q * 4
+    refresh = w.B * H_kv * (ps * D * 2 + 4 * D)  # a1: last page read, its summary written
+    return dict(attn=kv + qo, score=summ + w.B * w.H_q * D * 2, refresh=refresh,
+                step=kv + summ + qo + refresh)
+
+
+def verify_bytes(w, T):
+    return sum(int(w.seq_lens[b]) * w.H_kv * 4 * w.D for b in range(w.B)) + w.B * T * w.H_q * w.D * 4
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if ts < t0 - 0.06 or ts > t1 + 0.1:
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    import sparse_attention_decode_pages_gb300 as spd
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    # Each rank is an independent replica with its own seeded batch.
+    spec = wl.spec(args.config, args.page_size)
+    spec.seed += 100 * rank
+    if args.batch:
+        spec.B = args.batch
+    w = wl.make(spec)
+    T = w.T or 7
+    if w.q_verify is None:
+        rng = np.random.default_rng(spec.seed + 7)
+        w.q_verify = wl.f32_to_bf16_bits(rng.standard_normal((w.B, T, w.H_q, w.D)).astype(np.float32))
+    d = wl.to_device(w, dev)
+    dims = spd.dims_of(w.B, w.H_q, w.H_kv, w.D, w.page_size, w.max_pages_per_seq, w.num_phys_pages)
+    summ = torch.empty((w.num_phys_pages, w.H_kv, 2, w.D), dtype=torch.bfloat16, device=dev)
+    spd.pages_summarize(dims, d["K"], d["page_table"], d["seq_lens"], summ)  # prefill
+    last = torch.tensor([b * w.max_pages_per_seq + (int(w.seq_lens[b]) - 1) // w.page_size
+                         for b in range(w.B)], dtype=torch.int32, device=dev)
+    k_max = w.k_max
+    sel = torch.empty((w.B, w.H_kv, k_max), dtype=torch.int32, device=dev)
+    nsel = torch.empty((w.B, w.H_kv), dtype=torch.int32, device=dev)
+    o = torch.empty((w.B, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H_q), dtype=torch.float32, device=dev)
+    ov = torch.empty((w.B, T, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
+    lsev = torch.empty((w.B, T, w.H_q), dtype=torch.float32, device=dev)
+    ws_sel = spd.workspace(spd.spd_score_select_workspace_size(dims), dev)
+    ws_attn = spd.workspace(spd.spd_sparse_decode_workspace_size(dims, k_max, args.splits), dev)
+    ws_ver = spd.workspace(spd.spd_dense_verify_workspace_size(dims, T, args.vsplits), dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    policy = spd.policy_of(w.policy)
+
+    def sparse_pass(ev=None):
+        if ev:
+            ev[0].record(stream)
+        spd.pages_summarize(dims, d["K"], d["page_table"], d["seq_lens"], summ, only_pages=last)
+        if ev:
+            ev[1].record(stream)
+        spd.pages_score_select(dims, d["q"], summ, d["page_table"], d["seq_lens"], policy, sel,
+                               nsel, k_max, ws_sel)
+        if ev:
+            ev[2].record(stream)
+        spd.sparse_decode_attn(dims, d["q"], d["K"], d["V"], d["page_table"], d["seq_lens"], sel,
+                               nsel, k_max, o, ws_attn, lse=lse, num_splits=args.splits)
+        if ev:
+            ev[3].record(stream)
+
+    def verify_pass(ev=None):
+        if ev:
+            ev[0].record(stream)
+        spd.dense_verify_attn(dims, T, d["q_verify"], d["K"], d["V"], d["page_table"],
+                              d["seq_lens"], ov, ws_ver, lse=lsev, num_splits=args.vsplits)
+        if ev:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        sparse_pass()
+        flush.zero_()
+        verify_pass()
+        flush.zero_()
+    torch.cuda.synchronize()
+    status = spd.spd_device_status(clear=True)
+    if status:
+        raise RuntimeError(f"device status {status:#x} after warm-up")
+
+    nsel_host = nsel.cpu().numpy()
+    sel_host = sel.cpu().numpy()
+    chosen = [[sel_host[b, h, : nsel_host[b, h]].tolist() for h in range(w.H_kv)] for b in range(w.B)]
+    nbytes = algorithmic_bytes(w, chosen)
+    vbytes = verify_bytes(w, T)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    vevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        sparse_pass(evs[i])
+        flush.zero_()
+        verify_pass(vevs[i])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1)
+    status = spd.spd_device_status(clear=True)
+    if status:
+        raise RuntimeError(f"device status {status:#x} in the timed region")
+
+    t_ref = [e[0].elapsed_time(e[1]) for e in evs]
+    t_sel = [e[1].elapsed_time(e[2]) for e in evs]
+    t_att = [e[2].elapsed_time(e[3]) for e in evs]
+    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    t_ver = [e[0].elapsed_time(e[1]) for e in vevs]
+    ms_step = float(np.mean(t_step))
+    ms_ver = float(np.mean(t_ver))
+    ms_att = float(np.mean(t_att))
+
+    # e2e: the same sparse pass through the C ABI with host buffers.
+    q_h = d["q"].cpu().pin_memory()
+    sl_h = d["seq_lens"].cpu().pin_memory()
+    pt_h = d["page_table"].cpu().pin_memory()
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        d["q"].copy_(q_h, non_blocking=True)
+        d["seq_lens"].copy_(sl_h, non_blocking=True)
+        d["page_table"].copy_(pt_h, non_blocking=True)
+        sparse_pass()
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        eb.record(stream)
+        eb.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(ea.elapsed_time(eb))
+    h2d = q_h.numel() * 2 + sl_h.numel() * 4 + pt_h.numel() * 4
+    d2h = o_h.numel() * 2 + lse_h.numel() * 4
+
+    # max over ranks
+    vals = torch.tensor([ms_step, ms_ver, float(np.mean(e2e_ms)), ms_att], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    ms_step, ms_ver, ms_e2e, ms_att = [float(x) for x in vals.tolist()]
+
+    peak, peak_src = hbm_peak()
+    att_gbs = nbytes["attn"] / (ms_att * 1e-3) / 1e9
+    step_gbs = nbytes["step"] / (ms_step * 1e-3) / 1e9
+    ver_gbs = vbytes / (ms_ver * 1e-3) / 1e9
+    traffic = None
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            tr = json.load(fh)
+        ent = tr.get(f"sparse_decode_attn/{args.config}")
+        if ent and ent.get("source_hash") == kernel_source_hash():
+            traffic = ent["bytes_per_launch"]
+    except Exception:
+        pass
+
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = cpu_baseline(w, T)
+        line = {
+            "metric": METRIC,
+            "value": world * w.B / (ms_step * 1e-3),
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded; shapes of the Qwen3-8B rollout workload)",
+            "config": {
+                "workload": f"{args.config}: B={w.B}, Hq/Hkv={w.H_q}/{w.H_kv}, D={w.D}, "
+                            f"ps={w.page_size}, len {int(w.seq_lens.min())}..{int(w.seq_lens.max())}, "
+                            f"budget {w.policy.fixed_pages if w.policy.mode == 'fixed' else w.policy.mode} pages, "
+                            f"sink 1 + local {w.policy.local_pages}; verify T={T}",
+                "global_batch": world * w.B,
+                "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                "l2": "flushed between timed passes (256 MiB write, outside the events)",
+                "splits": args.splits, "verify_splits": args.vsplits,
+            },
+            "step_ms": {"a1_refresh": float(np.mean(t_ref)), "a2_a4_score_select": float(np.mean(t_sel)),
+                        "a5_a6_sparse_attn": ms_att},
+            "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s",
+                              "frac": step_gbs / peak, "bytes": nbytes["step"],
+                              "frac_of_nominal_8tbs": step_gbs / 8000.0},
+            "roofline": {"bound": "hbm", "kernel": "sparse_decode_attn", "achieved": att_gbs,
+                         "peak": peak, "unit": "GB/s", "frac": att_gbs / peak,
+                         "traffic": traffic, "algorithmic_bytes": nbytes["attn"],
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_src == "measured" else "fallback 6.8 TB/s"},
+            "dense_verify": {"tokens_per_s": world * w.B * T / (ms_ver * 1e-3), "ms": ms_ver,
+                             "achieved_gbs": ver_gbs, "frac": ver_gbs / peak, "bytes": vbytes,
+                             "tflops": 4.0 * sum(int(w.seq_lens[b]) for b in range(w.B)) * w.H_q * T * w.D
+                             / (ms_ver * 1e-3) / 1e12},
+            "e2e": {"value": world * w.B / (ms_e2e * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms": ms_e2e},
+            "gpu_launches": args.steps * 4,
+            "clocks": clocks,
+            "wall_s_timed_region": t1 - t0,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _oracle_sparse_step(w, summ, threads):
+    import oracle
+    sc = oracle.scores(w, summ, threads=threads)
+    sel, nsel = oracle.select(w, sc, threads=threads)
+    return oracle.sparse_attn(w, sel, nsel, threads=threads)
+
+
+def cpu_baseline(w, T, min_seconds=3.0):
+    """The fp64 oracle as it stands on the host cores: score + select + sparse attention."""
+    import oracle
+    threads = os.cpu_count() or 1
+    summ = oracle.summarize(w, threads=threads)  # prefill, outside the timing
+    n, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_sparse_step(w, summ, threads)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    return {"value": n * w.B / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} full passes of scores + selection + sparse attention over the whole "
+                      f"batch (B={w.B}); page summaries precomputed once outside the timing"}
+
+
+def run_reference(args):
+    """The oracle arm: rank 0 only; every step is one full pass over the batch."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+    w = wl.named(args.config, args.page_size)
+    threads = os.cpu_count() or 1
+    summ = oracle.summarize(w, threads=threads)
+    for _ in range(args.warmup):
+        _oracle_sparse_step(w, summ, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_sparse_step(w, summ, threads)
+    el = time.perf_counter() - t0
+    value = args.steps * w.B / el
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; shapes of the Qwen3-8B rollout workload)",
+        "config": {"workload": f"{args.config}: B={w.B}, Hq/Hkv={w.H_q}/{w.H_kv}, D={w.D}, "
+                               f"ps={w.page_size}", "global_batch": w.B,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{args.steps} passes of scores + selection + sparse attention "
+                                   f"over the whole batch; summaries precomputed"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", default="q8b", choices=["tiny", "q17b", "q8b", "sweep", "longtail"])
+    ap.add_argument("--page-size", type=int, default=None)
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--vsplits", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="override B (small profiling cases)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -428,8 +428,12 @@ template <int D, int PS, int NMT, bool SPARSE>
 int attn_ctas_per_sm_t() {
     using C = AttnCfg<D, PS, NMT>;
     int n = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<D, PS, NMT, SPARSE>, C::THREADS,
-                                                                  C::SMEM);
+    // The answer depends on the kernel's dynamic shared-memory limit: set it first
+    // so the split count is the same before and after the kernel's first launch.
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, PS, NMT, SPARSE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<D, PS, NMT, SPARSE>, C::THREADS, C::SMEM);
     if (e != cudaSuccess) return 1;
     return n > 0 ? n : 1;
 }

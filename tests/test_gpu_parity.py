@@ -268,3 +268,19 @@ def test_dense_all_pages_equals_sparse_all_pages():
     assert g.sync_status() == 0
     assert np.abs(np_bf16(o_s) - np_bf16(o_d)[:, 0]).max() <= 1e-2
     assert np.abs(lse_s.cpu().numpy() - lse_d.cpu().numpy()[:, 0]).max() <= 1e-3
+
+
+def test_workspace_sizes_do_not_change_after_first_launch():
+    """Auto split counts (and so workspace sizes) are the same before and after launches."""
+    w = small("q8b")
+    g = Gpu(w)
+    before = (g.spd.spd_sparse_decode_workspace_size(g.dims, w.k_max, 0),
+              g.spd.spd_dense_verify_workspace_size(g.dims, 7, 0))
+    summ = g.summarize()
+    sel, nsel, _, _ = g.score_select(summ)
+    g.sparse_attn(sel, nsel)
+    g.verify(7)
+    after = (g.spd.spd_sparse_decode_workspace_size(g.dims, w.k_max, 0),
+             g.spd.spd_dense_verify_workspace_size(g.dims, 7, 0))
+    assert before == after
+    assert g.sync_status() == 0
