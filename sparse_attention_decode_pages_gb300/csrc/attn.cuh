@@ -1,21 +1,36 @@
-// attn.cuh -- paged FlashDecoding kernel shared by sparse decode (attention over
-// the selected pages: Sparrow's block-sparse rollout attention, the S3R sparse
-// drafter) and dense causal verification (S3R "Verify (TV)": T drafted
-// positions over the complete KV cache).
+// attn.cuh -- persistent, warp-specialised paged FlashDecoding kernel shared by
+// sparse decode (attention over the selected pages only: Sparrow's
+// block-sparse rollout attention, the S3R sparse drafter) and dense causal
+// verification (S3R "Verify (TV)": T drafted positions over the complete KV
+// cache).
 //
-// One CTA per (sequence, KV head, split).  The CTA holds all R = T*G query
-// rows of the KV head (padded to 16-row MMA tiles) so the G grouped heads and T
-// positions share every page load.  Warps form NG page groups of NMT warps;
-// group g takes every NG-th item of the CTA's page range and owns a ring of
-// STAGES shared-memory slots.  For each page one lane issues TMA tensor loads
-// (cp.async.bulk.tensor, 128-byte swizzle, mbarrier transaction counts) of the
-// page's K and V tiles -- only the selected pages are ever fetched.  Compute
-// per 16-token chunk: S = Q K^T and O += P V on the tensor cores (mma.sync
-// m16n8k16 bf16 -> fp32; K and V tiles read with ldmatrix, conflict-free under
-// the swizzle), online softmax in fp32 with exp2.  The page groups are merged
-// in shared memory at the end.  With several splits per row the CTA writes a
-// normalised partial (o, lse) to the workspace and the last CTA of the row to
-// finish (atomic ticket; nothing waits) merges them with the log-sum-exp rule.
+// Work units.  A unit is a contiguous run of at most `items_per_split` pages
+// ("items") of one (sequence, KV head) row: the selected pages (sparse) or all
+// pages (dense).  A unit holds all R = T*G query rows of the KV head, padded to
+// 16-row MMA tiles, so the G grouped heads and T positions share each page
+// load.  Units are numbered row-major and handed out by an atomic queue.
+//
+// Workers.  A CTA is one worker: NMT consumer warps (one per 16-row tile) and
+// one producer warp, running until the queue is empty (a persistent grid sized
+// to the GPU).  The producer claims units, resolves 32 items at a time (the
+// selection entries and page-table lookups of a batch are one round trip),
+// and for each item waits for a free ring slot (an "empty" mbarrier the
+// consumers arrive on) and issues TMA tensor loads (cp.async.bulk.tensor,
+// 128-byte swizzle) of the page's K and V tiles; the first item of a unit also
+// carries a bulk copy of the unit's Q rows.  The item's logical page and unit
+// are written to shared memory before the producer arrives on the slot's
+// "full" mbarrier, so the consumers issue no global loads in their main loop
+// and the ring keeps streaming across unit boundaries while an epilogue runs.
+// The end of the work is signalled through the ring itself.
+//
+// Compute per 16-token chunk: S = Q K^T and O += P V on the tensor cores
+// (mma.sync m16n8k16 bf16 -> fp32, K / V read with ldmatrix, conflict-free
+// under the swizzle), online softmax in fp32 with exp2.  A unit that is a
+// whole row writes o / lse directly; otherwise it writes a normalised partial
+// and the last unit of the row to finish (an atomic ticket; nothing waits)
+// merges the partials with the log-sum-exp rule.  The last producer to run out
+// of units resets the queue, so the workspace counters are zero again on exit.
+// Every wait is bounded (SPD_DEV_TIMEOUT on expiry).
 #pragma once
 
 #include "common.cuh"
@@ -23,192 +38,279 @@
 
 namespace spd {
 
-template <int D, int PS, int NMT>
-struct AttnCfg;
+struct UnitInfo {
+    int row;     // b * H_kv + h
+    int split;   // index of this unit within the row
+    int start;   // first item
+    int count;   // items
+    int len;     // seq_lens[b]
+    int nsplit;  // units of this row
+};
 
-// Page groups and ring depth: about 64-96 KB of ring per CTA.
 template <int D, int PS, int NMT>
 struct AttnCfg {
     static constexpr int TILE = PS * D * 2;  // bytes of one K (or V) tile
     static constexpr int SLOT = 2 * TILE;
-    static constexpr int NG_BASE = (SLOT <= 8192) ? 4 : (SLOT <= 16384 ? 2 : 1);
-    static constexpr int NG = (NG_BASE / NMT) > 0 ? (NG_BASE / NMT) : 1;
-    static constexpr int STAGES = (SLOT <= 4096) ? 4 : 3;
-    static constexpr int THREADS = NG * NMT * 32;
-    static constexpr int RP = NMT * 16;  // padded rows
-    static constexpr int RING = NG * STAGES * SLOT;
-    static constexpr int EPI = NG * RP * (D + 2) * 4;
-    static constexpr int BODY = RING > EPI ? RING : EPI;
-    static constexpr int SMEM = 1024 /*alignment slack*/ + BODY + NG * STAGES * 8;
+    // ring depth: ~24-64 KB of K/V in flight per worker
+    static constexpr int STAGES = NMT == 1 ? (SLOT <= 8192 ? 3 : 2) : (SLOT <= 8192 ? 4 : (SLOT <= 16384 ? 3 : 2));
+    static constexpr int THREADS = (NMT + 1) * 32;  // consumers + one producer warp
+    static constexpr int RP = NMT * 16;             // padded rows
+    static constexpr int QBYTES = RP * D * 2;
+    static constexpr int NQ = STAGES + 1;           // Q buffers: at most STAGES + 1 units are live
+    static constexpr int FIFO = 8;                  // unit-info entries (>= STAGES + 1)
+    static constexpr int OFF_Q = STAGES * SLOT;
+    static constexpr int OFF_BAR = OFF_Q + NQ * QBYTES;          // full[STAGES], empty[STAGES]
+    static constexpr int OFF_FIFO = OFF_BAR + 2 * STAGES * 8;
+    static constexpr int OFF_META = OFF_FIFO + FIFO * (int)sizeof(UnitInfo);  // int2 per slot
+    static constexpr int BODY = OFF_META + STAGES * 8;
+    static constexpr int SMEM = 1024 /*alignment slack*/ + BODY;
+    static_assert(STAGES + 1 <= NQ && STAGES + 1 <= FIFO, "ring deeper than the unit buffers");
 };
+
+constexpr int kEndOfWork = -2;  // slot_meta.x: no more items
+constexpr float kRescale = 8.f;  // log2 headroom before the running max moves
 
 template <int D, int PS, int NMT, bool SPARSE>
 __global__ void __launch_bounds__(AttnCfg<D, PS, NMT>::THREADS)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV) {
     using C = AttnCfg<D, PS, NMT>;
-    constexpr int NG = C::NG, STAGES = C::STAGES, RP = C::RP;
+    constexpr int STAGES = C::STAGES;
     constexpr int KSTEPS = D / 16;
     constexpr int NT_O = D / 8;
     constexpr int HALVES = D / 64;
     constexpr int HALF_BYTES = PS * 128;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ int s_last;
+    __shared__ int s_flag;
 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BODY);
+    uint8_t* ring = smem;
+    uint8_t* qbuf = smem + C::OFF_Q;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* empty = full + STAGES;
+    UnitInfo* fifo = reinterpret_cast<UnitInfo*>(smem + C::OFF_FIFO);
+    int2* slot_meta = reinterpret_cast<int2*>(smem + C::OFF_META);  // {logical page or -1 / end, unit seq}
 
-    const int b = blockIdx.z, h = blockIdx.y, split = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int grp = warp / NMT, mt = warp % NMT;
     const int G = a.H_q / a.H_kv;
     const int R = a.T * G;
-    const int len = a.seq_lens[b];
-    const int P = (len + PS - 1) / PS;
+    const float NEG_INF = __int_as_float(0xff800000);
 
-    int n_items;
-    const int32_t* sel_row = nullptr;
-    if (SPARSE) {
-        sel_row = a.sel + ((long long)b * a.H_kv + h) * a.k_max;
-        n_items = a.nsel[(long long)b * a.H_kv + h];
-        if (n_items > a.k_max || n_items < 0) {
-            if (tid == 0) raise_status(a.status, SPD_DEV_BAD_SEL);
-            n_items = n_items < 0 ? 0 : a.k_max;
+    // Padding rows of the Q buffers stay zero; only the R real rows are copied.
+    for (int i = tid; i < C::NQ * C::QBYTES / 16; i += C::THREADS)
+        reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
+    if (tid == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(full + i, 1);
+            mbar_init(empty + i, NMT);
         }
-    } else {
-        n_items = P;
+        mbar_fence_init();
     }
-    const int nsplit_row = (n_items + a.items_per_split - 1) / a.items_per_split;
-    const long long row0 = ((long long)b * a.H_kv + h);  // (b, h) index
+    // generic-proxy zeros of the Q buffers before any bulk copy into them
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
 
-    // Output row r -> (t, g): o index ((b*T + t)*H_q + h*G + g)*D.
-    auto out_index = [&](int r) -> long long {
+    // Output row r of a (b, h) row -> index into o ([B][T][H_q]) and lse.
+    auto out_index = [&](int bh, int r) -> long long {
+        const int b = bh / a.H_kv, h = bh - b * a.H_kv;
         const int t = r / G, g = r - t * G;
         return ((long long)b * a.T + t) * a.H_q + h * G + g;
     };
 
-    if (split >= nsplit_row) {
-        if (split == 0) {  // empty row: o = 0, lse = -inf
-            for (int i = tid; i < R * D; i += C::THREADS) {
-                const int r = i / D, d = i - r * D;
-                reinterpret_cast<bf16*>(a.o)[out_index(r) * D + d] = __float2bfloat16(0.f);
+    if (warp == NMT) {
+        // ============================================================ producer warp
+        if (lane == 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+        }
+        const long long total_units = (long long)a.B * a.H_kv * a.num_splits;
+        int* queue = a.queue;  // [0..1] 64-bit unit counter, [2] producers finished
+        long long j = 0;       // items issued
+        int seq = 0;           // units issued
+        bool ok = true;
+        // Waits (lane 0) until slot j % STAGES is free; false if the wait ran out.
+        auto slot_free = [&](long long jj) -> bool {
+            bool r = true;
+            if (lane == 0 && jj >= STAGES)
+                r = mbar_wait_bounded(empty + (jj % STAGES), (uint32_t)(((jj / STAGES) - 1) & 1), a.status);
+            return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+        };
+        while (ok) {
+            unsigned long long u = 0;
+            if (lane == 0) u = atomicAdd(reinterpret_cast<unsigned long long*>(queue), 1ull);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if ((long long)u >= total_units) break;
+            const int row = (int)(u / a.num_splits), split = (int)(u % a.num_splits);
+            const int b = row / a.H_kv, h = row - b * a.H_kv;
+            const int len = a.seq_lens[b];
+            const int P = (len + PS - 1) / PS;
+            int n_items;
+            if (SPARSE) {
+                n_items = a.nsel[row];
+                if (n_items < 0 || n_items > a.k_max) {
+                    if (lane == 0) raise_status(a.status, SPD_DEV_BAD_SEL);
+                    n_items = n_items < 0 ? 0 : a.k_max;
+                }
+            } else {
+                n_items = P;
             }
-            if (a.lse)
-                for (int r = tid; r < R; r += C::THREADS) a.lse[out_index(r)] = __int_as_float(0xff800000);
+            const int start = split * a.items_per_split;
+            const int count = min(a.items_per_split, n_items - start);
+            if (count <= 0) {
+                if (split == 0)  // empty row: o = 0, lse = -inf
+                    for (int i = lane; i < R * (D / 8); i += 32) {
+                        const int r = i / (D / 8), d = (i % (D / 8)) * 8;
+                        const long long oi = out_index(row, r);
+                        *reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(a.o) + oi * D + d) = make_uint4(0, 0, 0, 0);
+                        if (d == 0 && a.lse) a.lse[oi] = NEG_INF;
+                    }
+                continue;
+            }
+            if (lane == 0) {
+                UnitInfo info;
+                info.row = row;
+                info.split = split;
+                info.start = start;
+                info.count = count;
+                info.len = len;
+                info.nsplit = (n_items + a.items_per_split - 1) / a.items_per_split;
+                fifo[seq % C::FIFO] = info;  // published by the first item's arrive (release)
+            }
+            for (int base = 0; base < count && ok; base += 32) {
+                // resolve 32 items in one round trip
+                int lp = -1;
+                long long phys = -1;
+                if (base + lane < count) {
+                    const int it = start + base + lane;
+                    lp = SPARSE ? a.sel[(long long)row * a.k_max + it] : it;
+                    if (lp < 0 || lp >= P) {
+                        raise_status(a.status, SPD_DEV_BAD_SEL);
+                        lp = -1;
+                    } else {
+                        phys = a.page_table[(long long)b * a.max_pages + lp];
+                        if (phys < 0 || phys >= a.num_phys) {
+                            raise_status(a.status, SPD_DEV_BAD_PAGE);
+                            lp = -1;
+                        }
+                    }
+                }
+                const int nb = min(32, count - base);
+                for (int k = 0; k < nb; ++k) {
+                    const int lpk = __shfl_sync(0xffffffffu, lp, k);
+                    const long long pk = __shfl_sync(0xffffffffu, phys, k);
+                    if (!slot_free(j)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        const int slot = (int)(j % STAGES);
+                        slot_meta[slot] = make_int2(lpk, seq);
+                        const bool first = (base + k == 0);
+                        uint32_t bytes = lpk >= 0 ? (uint32_t)C::SLOT : 0u;
+                        if (first) bytes += (uint32_t)(R * D * 2);
+                        mbar_arrive_expect_tx(full + slot, bytes);
+                        if (first) {  // the unit's Q rows: T runs of G*D contiguous bf16
+                            uint8_t* qd = qbuf + (seq % C::NQ) * C::QBYTES;
+                            const bf16* qs = reinterpret_cast<const bf16*>(a.q);
+                            for (int t = 0; t < a.T; ++t)
+                                bulk_load(qd + t * G * D * 2, qs + (((long long)b * a.T + t) * a.H_q + h * G) * D,
+                                          (uint32_t)(G * D * 2), full + slot);
+                        }
+                        if (lpk >= 0) {
+                            uint8_t* dst = ring + slot * C::SLOT;
+                            const int y = (int)((pk * a.H_kv + h) * PS);
+#pragma unroll
+                            for (int hf = 0; hf < HALVES; ++hf) {
+                                tma_load_2d(dst + hf * HALF_BYTES, &tmK, hf * 64, y, full + slot);
+                                tma_load_2d(dst + C::TILE + hf * HALF_BYTES, &tmV, hf * 64, y, full + slot);
+                            }
+                        }
+                    }
+                    ++j;
+                }
+            }
+            ++seq;
+        }
+        // End of work, signalled through the ring.
+        if (ok && slot_free(j) && lane == 0) {
+            const int slot = (int)(j % STAGES);
+            slot_meta[slot] = make_int2(kEndOfWork, seq);
+            mbar_arrive_expect_tx(full + slot, 0);
+        }
+        // The last producer to finish resets the queue for the next call.
+        if (lane == 0) {
+            __threadfence();
+            const unsigned prev = atomicAdd(reinterpret_cast<unsigned*>(queue + 2), 1u);
+            if (prev == gridDim.x - 1) {
+                *reinterpret_cast<unsigned long long*>(queue) = 0ull;
+                queue[2] = 0;
+                __threadfence();
+            }
         }
         return;
     }
-    const int it_begin = split * a.items_per_split;
-    const int it_end = min(n_items, it_begin + a.items_per_split);
-    // items of this group: it_begin + grp + NG*j
-    const int n_g = (it_end - it_begin - grp + NG - 1) / NG > 0 ? (it_end - it_begin - grp + NG - 1) / NG : 0;
 
-    const bool producer = (mt == 0) && (lane == 0);
-    uint8_t* ring = smem + grp * STAGES * C::SLOT;
-    uint64_t* gbar = bars + grp * STAGES;
-
-    if (tid == 0) {
-        for (int i = 0; i < NG * STAGES; ++i) mbar_init(bars + i, 1);
-        mbar_fence_init();
-    }
-    if (tid == 32 % C::THREADS) {
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-    }
-    __syncthreads();
-
-    // Item j of this group -> logical page and physical page; -1 (and the
-    // status bit to raise) when the selection entry or the page id is bad.
-    auto item_page = [&](int j, long long& phys, unsigned& err) -> int {
-        const int it = it_begin + grp + NG * j;
-        const int lp = SPARSE ? sel_row[it] : it;
-        phys = -1;
-        if (lp < 0 || lp >= P) {
-            err = SPD_DEV_BAD_SEL;
-            return -1;
-        }
-        const long long f = a.page_table[(long long)b * a.max_pages + lp];
-        if (f < 0 || f >= a.num_phys) {
-            err = SPD_DEV_BAD_PAGE;
-            return -1;
-        }
-        phys = f;
-        err = 0;
-        return lp;
-    };
-    auto issue = [&](int j) {
-        const int slot = j % STAGES;
-        long long phys;
-        unsigned err;
-        const int lp = item_page(j, phys, err);
-        uint8_t* dst = ring + slot * C::SLOT;
-        if (lp < 0) {
-            raise_status(a.status, err);
-            mbar_arrive_expect_tx(gbar + slot, 0);  // completes the phase with no data
-            return;
-        }
-        mbar_arrive_expect_tx(gbar + slot, C::SLOT);
-        const int y = (int)((phys * a.H_kv + h) * PS);
-#pragma unroll
-        for (int hf = 0; hf < HALVES; ++hf) {
-            tma_load_2d(dst + hf * HALF_BYTES, &tmK, hf * 64, y, gbar + slot);
-            tma_load_2d(dst + C::TILE + hf * HALF_BYTES, &tmV, hf * 64, y, gbar + slot);
-        }
-    };
-    if (producer) {
-        for (int j = 0; j < n_g && j < STAGES; ++j) issue(j);
-    }
-
-    // Q fragments (A operand) for this warp's 16 rows.
+    // ============================================================ consumer warps
+    const int mt = warp;
     const int qr0 = mt * 16 + (lane >> 2), qr1 = qr0 + 8;
     const int c4 = lane & 3;
     uint32_t qa[KSTEPS][4];
-    {
-        const bf16* qb = reinterpret_cast<const bf16*>(a.q);
-        const bf16* q0 = qr0 < R ? qb + out_index(qr0) * D : nullptr;
-        const bf16* q1 = qr1 < R ? qb + out_index(qr1) * D : nullptr;
-#pragma unroll
-        for (int kk = 0; kk < KSTEPS; ++kk) {
-            const int d0 = kk * 16 + 2 * c4;
-            qa[kk][0] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + d0) : 0u;
-            qa[kk][1] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + d0) : 0u;
-            qa[kk][2] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + d0 + 8) : 0u;
-            qa[kk][3] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + d0 + 8) : 0u;
-        }
-    }
-    // Last visible absolute position of each of this thread's rows.
-    const int lim0 = qr0 < R ? len - a.T + qr0 / G : len - 1;
-    const int lim1 = qr1 < R ? len - a.T + qr1 / G : len - 1;
-    const int lim_min = len - a.T;  // smallest limit among real rows
-
-    const float NEG_INF = __int_as_float(0xff800000);
     float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
     float oacc[NT_O][4];
-#pragma unroll
-    for (int i = 0; i < NT_O; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+    int lim0 = 0, lim1 = 0, lim_min = 0;
+    UnitInfo cu;
+    cu.count = 0;
+    int cur_seq = -1, c_item = 0;
+    // consumer-only barrier (the producer warp never joins it)
+    auto consumers_sync = [&]() {
+        if (NMT > 1)
+            asm volatile("bar.sync 1, %0;" ::"r"(NMT * 32) : "memory");
+        else
+            __syncwarp();
+    };
 
-    bool ok = true;
-    for (int j = 0; j < n_g; ++j) {
-        const int slot = j % STAGES;
-        const uint32_t parity = (uint32_t)((j / STAGES) & 1);
-        bool got = ok && mbar_wait_bounded(gbar + slot, parity, a.status);
-        long long phys;
-        unsigned err;
-        const int lp = item_page(j, phys, err);
-        if (got && lp >= 0) {
+    for (long long j = 0;; ++j) {
+        const int slot = (int)(j % STAGES);
+        if (!mbar_wait_bounded(full + slot, (uint32_t)((j / STAGES) & 1), a.status)) break;
+        const int2 meta = slot_meta[slot];
+        if (meta.x == kEndOfWork) break;
+        if (meta.y != cur_seq) {
+            // new unit: its info, Q fragments, fresh softmax state, row limits
+            cur_seq = meta.y;
+            cu = fifo[cur_seq % C::FIFO];
+            c_item = 0;
+            const uint8_t* qsm = qbuf + (cur_seq % C::NQ) * C::QBYTES;
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                const int d0 = kk * 16 + 2 * c4;
+                qa[kk][0] = *reinterpret_cast<const uint32_t*>(qsm + (qr0 * D + d0) * 2);
+                qa[kk][1] = *reinterpret_cast<const uint32_t*>(qsm + (qr1 * D + d0) * 2);
+                qa[kk][2] = *reinterpret_cast<const uint32_t*>(qsm + (qr0 * D + d0 + 8) * 2);
+                qa[kk][3] = *reinterpret_cast<const uint32_t*>(qsm + (qr1 * D + d0 + 8) * 2);
+            }
+            m0 = m1 = NEG_INF;
+            l0 = l1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < NT_O; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+            lim0 = qr0 < R ? cu.len - a.T + qr0 / G : cu.len - 1;
+            lim1 = qr1 < R ? cu.len - a.T + qr1 / G : cu.len - 1;
+            lim_min = cu.len - a.T;
+        }
+        const int lp = meta.x;
+        if (lp >= 0) {
             uint8_t* kt = ring + slot * C::SLOT;
             uint8_t* vt = kt + C::TILE;
             const int page_start = lp * PS;
             // Slots past the sequence end may hold anything (even NaN): zero them in V.
-            const int valid = min(PS, len - page_start);
+            const int valid = min(PS, cu.len - page_start);
             if (valid < PS) {
                 for (int i = lane; i < (PS - valid) * HALVES * 8; i += 32) {
                     const int rr = valid + i / (HALVES * 8);
                     const int rem = i % (HALVES * 8);
-                    const int hf = rem / 8, ch = rem % 8;
-                    *reinterpret_cast<uint4*>(vt + hf * HALF_BYTES + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(vt + (rem / 8) * HALF_BYTES + rr * 128 + (rem % 8) * 16) =
+                        make_uint4(0, 0, 0, 0);
                 }
-                // order these generic-proxy writes before the slot's next TMA refill
+                // order these generic-proxy writes before the producer's next TMA into the slot
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
             }
@@ -231,7 +333,6 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT>::THREADS)
                         mma_bf16(s[1], qa[kk], b2, b3);
                     }
                 }
-                // scale to log2 units, mask, online softmax
                 const int tok0 = page_start + cc * 16;
                 const bool need_mask = tok0 + 15 > lim_min;
 #pragma unroll
@@ -255,12 +356,29 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT>::THREADS)
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float base0 = mn0 == NEG_INF ? 0.f : mn0;
-                const float base1 = mn1 == NEG_INF ? 0.f : mn1;
-                const float al0 = fast_exp2(m0 - base0), al1 = fast_exp2(m1 - base1);
-                m0 = mn0;
-                m1 = mn1;
+                // Lazy rescaling: the running max (the exponent base) only moves when a
+                // logit exceeds it by more than 2^8 (kRescale in log2 units), so most
+                // chunks skip rescaling O; terms stay <= 2^8, harmless in fp32.
+                const bool up0 = mx0 > m0 + kRescale, up1 = mx1 > m1 + kRescale;
+                float al0 = 1.f, al1 = 1.f;
+                if (__any_sync(0xffffffffu, up0 || up1)) {
+                    const float mn0 = up0 ? mx0 : m0, mn1 = up1 ? mx1 : m1;
+                    al0 = (m0 == NEG_INF) ? 0.f : fast_exp2(m0 - mn0);
+                    al1 = (m1 == NEG_INF) ? 0.f : fast_exp2(m1 - mn1);
+                    m0 = mn0;
+                    m1 = mn1;
+                    l0 *= al0;
+                    l1 *= al1;
+#pragma unroll
+                    for (int i = 0; i < NT_O; ++i) {
+                        oacc[i][0] *= al0;
+                        oacc[i][1] *= al0;
+                        oacc[i][2] *= al1;
+                        oacc[i][3] *= al1;
+                    }
+                }
+                const float base0 = m0 == NEG_INF ? 0.f : m0;
+                const float base1 = m1 == NEG_INF ? 0.f : m1;
                 float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
@@ -271,15 +389,8 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT>::THREADS)
                     ps0 += s[nt][0] + s[nt][1];
                     ps1 += s[nt][2] + s[nt][3];
                 }
-                l0 = l0 * al0 + ps0;
-                l1 = l1 * al1 + ps1;
-#pragma unroll
-                for (int i = 0; i < NT_O; ++i) {
-                    oacc[i][0] *= al0;
-                    oacc[i][1] *= al0;
-                    oacc[i][2] *= al1;
-                    oacc[i][3] *= al1;
-                }
+                l0 += ps0;
+                l1 += ps1;
                 const uint32_t pa[4] = {pack_bf16(s[0][0], s[0][1]), pack_bf16(s[0][2], s[0][3]),
                                         pack_bf16(s[1][0], s[1][1]), pack_bf16(s[1][2], s[1][3])};
                 {
@@ -297,131 +408,118 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT>::THREADS)
                 }
             }
         }
-        // The whole group agrees on abort, and is done reading the slot.
-        bool bad = !got;
-        if (NMT == 1) {
-            bad = __any_sync(0xffffffffu, bad);
-        } else {
-            uint32_t any;
-            asm volatile(
-                "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-                "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-                : "=r"(any)
-                : "r"((uint32_t)bad), "r"(1 + grp), "r"(NMT * 32)
-                : "memory");
-            bad = any != 0;
-        }
-        if (bad) {
-            ok = false;
-            // Let the copies this group already issued land (bounded) before leaving.
-            if (producer)
-                for (int k2 = j + 1; k2 < n_g && k2 < j + STAGES; ++k2)
-                    mbar_wait_bounded(gbar + (k2 % STAGES), (uint32_t)((k2 / STAGES) & 1), a.status);
-            break;
-        }
-        if (producer && j + STAGES < n_g) issue(j + STAGES);
-    }
+        // This warp is done with the slot.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + slot);
+        if (++c_item < cu.count) continue;
 
-    // Row sums over the quad.
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-
-    // Merge the page groups through shared memory (the ring is idle now).
-    __syncthreads();
-    float* eo = reinterpret_cast<float*>(smem);             // [NG][RP][D]
-    float* em = eo + NG * RP * D;                            // [NG][RP]
-    float* el = em + NG * RP;                                // [NG][RP]
-    {
-        float* eg = eo + (grp * RP) * D;
+        // ---------------------------------------------------------- unit epilogue
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+        const float lse0 = l0 > 0.f ? (m0 + __log2f(l0)) * kLn2 : NEG_INF;
+        const float lse1 = l1 > 0.f ? (m1 + __log2f(l1)) * kLn2 : NEG_INF;
+        if (cu.nsplit == 1) {
+#pragma unroll
+            for (int i = 0; i < NT_O; ++i) {
+                const int d = i * 8 + 2 * c4;
+                if (qr0 < R)
+                    *reinterpret_cast<uint32_t*>(reinterpret_cast<bf16*>(a.o) + out_index(cu.row, qr0) * D + d) =
+                        pack_bf16(oacc[i][0] * inv0, oacc[i][1] * inv0);
+                if (qr1 < R)
+                    *reinterpret_cast<uint32_t*>(reinterpret_cast<bf16*>(a.o) + out_index(cu.row, qr1) * D + d) =
+                        pack_bf16(oacc[i][2] * inv1, oacc[i][3] * inv1);
+            }
+            if (c4 == 0 && a.lse) {
+                if (qr0 < R) a.lse[out_index(cu.row, qr0)] = lse0;
+                if (qr1 < R) a.lse[out_index(cu.row, qr1)] = lse1;
+            }
+            continue;
+        }
+        const long long pbase = ((long long)cu.row * a.num_splits + cu.split) * R;
 #pragma unroll
         for (int i = 0; i < NT_O; ++i) {
             const int d = i * 8 + 2 * c4;
-            *reinterpret_cast<float2*>(eg + qr0 * D + d) = make_float2(oacc[i][0], oacc[i][1]);
-            *reinterpret_cast<float2*>(eg + qr1 * D + d) = make_float2(oacc[i][2], oacc[i][3]);
+            if (qr0 < R)
+                *reinterpret_cast<float2*>(a.part_o + (pbase + qr0) * D + d) =
+                    make_float2(oacc[i][0] * inv0, oacc[i][1] * inv0);
+            if (qr1 < R)
+                *reinterpret_cast<float2*>(a.part_o + (pbase + qr1) * D + d) =
+                    make_float2(oacc[i][2] * inv1, oacc[i][3] * inv1);
         }
         if (c4 == 0) {
-            em[grp * RP + qr0] = m0;
-            em[grp * RP + qr1] = m1;
-            el[grp * RP + qr0] = l0;
-            el[grp * RP + qr1] = l1;
+            if (qr0 < R) a.part_lse[pbase + qr0] = lse0;
+            if (qr1 < R) a.part_lse[pbase + qr1] = lse1;
         }
-    }
-    __syncthreads();
-
-    const bool final_out = (nsplit_row == 1);
-    float* po = a.part_o + ((row0 * a.num_splits + split) * (long long)R) * D;
-    float* pl = a.part_lse + (row0 * a.num_splits + split) * (long long)R;
-    for (int i = tid; i < R * D; i += C::THREADS) {
-        const int r = i / D, d = i - r * D;
-        float M = NEG_INF;
+        // Ticket: the partial writes of every consumer lane are ordered before one
+        // acq_rel atomic (barrier, then release at GPU scope); the last unit of
+        // the row sees every other unit's partials through the acquire.
+        consumers_sync();
+        if (tid == 0) s_flag = (atomic_add_acq_rel(a.counters + cu.row, 1) == cu.nsplit - 1);
+        consumers_sync();
+        const bool last = s_flag != 0;
+        consumers_sync();  // s_flag is reused by the next unit
+        if (!last) continue;
+        // Last unit of the row: merge the partials of this warp's rows.  Lane s
+        // holds split s's lse; each lane owns D/32 consecutive channels, and the
+        // loads of a split are independent of each other.
+        const long long rbase = (long long)cu.row * a.num_splits * R;
+        constexpr int DPL = D / 32;  // channels per lane
+        for (int r = mt * 16; r < min(R, mt * 16 + 16); ++r) {
+            float M = NEG_INF;
+            for (int s0 = 0; s0 < cu.nsplit; s0 += 32)
+                if (s0 + lane < cu.nsplit) M = fmaxf(M, __ldcg(a.part_lse + rbase + (long long)(s0 + lane) * R + r));
 #pragma unroll
-        for (int g = 0; g < NG; ++g) M = fmaxf(M, em[g * RP + r]);
-        float L = 0.f, acc = 0.f;
-        if (M != NEG_INF) {
-#pragma unroll
-            for (int g = 0; g < NG; ++g) {
-                const float w = fast_exp2(em[g * RP + r] - M);
-                L += w * el[g * RP + r];
-                acc += w * eo[(g * RP + r) * D + d];
-            }
-        }
-        const float ov = L > 0.f ? acc / L : 0.f;
-        const float lv = L > 0.f ? (M + __log2f(L)) * kLn2 : NEG_INF;
-        if (final_out) {
-            reinterpret_cast<bf16*>(a.o)[out_index(r) * D + d] = __float2bfloat16(ov);
-            if (d == 0 && a.lse) a.lse[out_index(r)] = lv;
-        } else {
-            po[(long long)r * D + d] = ov;
-            if (d == 0) pl[r] = lv;
-        }
-    }
-    if (final_out) return;
-
-    // Split-K: the last CTA of the row merges the partials.
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const int prev = atomicAdd(a.counters + row0, 1);
-        s_last = (prev == nsplit_row - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    const float* pob = a.part_o + (row0 * a.num_splits) * (long long)R * D;
-    const float* plb = a.part_lse + (row0 * a.num_splits) * (long long)R;
-    for (int i = tid; i < R * D; i += C::THREADS) {
-        const int r = i / D, d = i - r * D;
-        float M = NEG_INF;
-        for (int s2 = 0; s2 < nsplit_row; ++s2) M = fmaxf(M, __ldcg(plb + (long long)s2 * R + r));
-        float ov = 0.f, lv = NEG_INF;
-        if (M != NEG_INF) {
+            for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
             float L = 0.f;
-            for (int s2 = 0; s2 < nsplit_row; ++s2) L += __expf(__ldcg(plb + (long long)s2 * R + r) - M);
-            const float lse_all = M + __logf(L);
-            for (int s2 = 0; s2 < nsplit_row; ++s2) {
-                const float ls = __ldcg(plb + (long long)s2 * R + r);
-                if (ls != NEG_INF) ov += __expf(ls - lse_all) * __ldcg(pob + ((long long)s2 * R + r) * D + d);
+            if (M != NEG_INF)
+                for (int s0 = 0; s0 < cu.nsplit; s0 += 32)
+                    if (s0 + lane < cu.nsplit) L += __expf(__ldcg(a.part_lse + rbase + (long long)(s0 + lane) * R + r) - M);
+#pragma unroll
+            for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+            const float lse_all = M == NEG_INF ? NEG_INF : M + __logf(L);
+            float acc[DPL];
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+            if (M != NEG_INF) {
+                for (int s0 = 0; s0 < cu.nsplit; s0 += 32) {
+                    const int ns = min(32, cu.nsplit - s0);
+                    float wl = 0.f;
+                    if (lane < ns) {
+                        const float ls = __ldcg(a.part_lse + rbase + (long long)(s0 + lane) * R + r);
+                        wl = ls == NEG_INF ? 0.f : __expf(ls - lse_all);
+                    }
+#pragma unroll 4
+                    for (int k = 0; k < ns; ++k) {
+                        const float wk = __shfl_sync(0xffffffffu, wl, k);
+                        const float* src = a.part_o + (rbase + (long long)(s0 + k) * R + r) * D + lane * DPL;
+                        if (DPL == 4) {
+                            const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+                            acc[0] += wk * v.x;
+                            acc[1 % DPL] += wk * v.y;
+                            acc[2 % DPL] += wk * v.z;
+                            acc[3 % DPL] += wk * v.w;
+                        } else {
+                            const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+                            acc[0] += wk * v.x;
+                            acc[1 % DPL] += wk * v.y;
+                        }
+                    }
+                }
             }
-            lv = lse_all;
+            const long long oi = out_index(cu.row, r);
+            bf16* dst = reinterpret_cast<bf16*>(a.o) + oi * D + lane * DPL;
+            if (DPL == 4) {
+                *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(acc[0], acc[1 % DPL]), pack_bf16(acc[2 % DPL], acc[3 % DPL]));
+            } else {
+                *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0], acc[1 % DPL]);
+            }
+            if (lane == 0 && a.lse) a.lse[oi] = lse_all;
         }
-        reinterpret_cast<bf16*>(a.o)[out_index(r) * D + d] = __float2bfloat16(ov);
-        if (d == 0 && a.lse) a.lse[out_index(r)] = lv;
+        if (tid == 0) a.counters[cu.row] = 0;
     }
-    if (tid == 0) a.counters[row0] = 0;
-}
-
-template <int D, int PS, int NMT, bool SPARSE>
-cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                          cudaStream_t st) {
-    using C = AttnCfg<D, PS, NMT>;
-    auto kern = attn_kernel<D, PS, NMT, SPARSE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    dim3 grid(a.num_splits, a.H_kv, a.B), block(C::THREADS);
-    kern<<<grid, block, C::SMEM, st>>>(a, tmK, tmV);
-    return cudaGetLastError();
 }
 
 template <int D, int PS, int NMT, bool SPARSE>
@@ -429,13 +527,27 @@ int attn_ctas_per_sm_t() {
     using C = AttnCfg<D, PS, NMT>;
     int n = 0;
     // The answer depends on the kernel's dynamic shared-memory limit: set it first
-    // so the split count is the same before and after the kernel's first launch.
+    // so the launch shape is the same before and after the kernel's first launch.
     cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, PS, NMT, SPARSE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<D, PS, NMT, SPARSE>, C::THREADS, C::SMEM);
     if (e != cudaSuccess) return 1;
     return n > 0 ? n : 1;
+}
+
+template <int D, int PS, int NMT, bool SPARSE>
+cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                          cudaStream_t st) {
+    using C = AttnCfg<D, PS, NMT>;
+    auto kern = attn_kernel<D, PS, NMT, SPARSE>;
+    const int per_sm = attn_ctas_per_sm_t<D, PS, NMT, SPARSE>();
+    const long long units = (long long)a.B * a.H_kv * a.num_splits;
+    long long grid = (long long)a.num_sms * per_sm;
+    if (grid > units) grid = units;
+    if (grid < 1) grid = 1;
+    kern<<<(unsigned)grid, C::THREADS, C::SMEM, st>>>(a, tmK, tmV);
+    return cudaGetLastError();
 }
 
 }  // namespace spd

@@ -56,9 +56,11 @@ struct AttnArgs {
     float scale_log2;
     uint16_t* o;
     float* lse;
-    float* part_o;
-    float* part_lse;
-    int* counters;
+    float* part_o;    // [B*H_kv][num_splits][R][D]
+    float* part_lse;  // [B*H_kv][num_splits][R]
+    int* counters;    // [B*H_kv] split tickets, zero on entry and on exit
+    int* queue;       // 16 bytes (8-aligned): unit queue + finished workers, zero on entry and exit
+    int num_sms;
     unsigned* status;
 };
 // Rows (T * G) handled per CTA, padded to 16-row MMA tiles.

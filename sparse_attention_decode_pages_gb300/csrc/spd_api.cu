@@ -128,55 +128,56 @@ spd_status check_dims(const spd_dims* d) {
 
 int pages_per_split_floor(int ps) { return ps >= 64 ? 2 : (ps == 32 ? 4 : 8); }
 
-// Splits of a selected-page list: enough CTAs for ~2 waves of the GPU, with at
-// least a few pages per split.
-int sparse_splits(const spd_dims* d, int k_max, int req, int sms) {
+// Splits per row: several units per persistent worker (units_per_worker), with
+// at least a few pages per unit, so the atomic unit queue balances the workers
+// and the last unit to finish is short.
+int splits_for(long long rows, int items, long long workers, int floor_items, int units_per_worker, int req) {
     int S = req;
     if (S <= 0) {
-        const long long rows = (long long)d->B * d->H_kv;
-        const long long slots = (long long)sms * occ_sparse_attn(d->D, d->page_size);
-        const int floor_items = pages_per_split_floor(d->page_size);
-        S = 1;
-        while (rows * S < 2 * slots && (k_max + 2 * S - 1) / (2 * S) >= floor_items) S *= 2;
+        const long long target = units_per_worker * workers;
+        S = (int)((target + rows - 1) / (rows > 0 ? rows : 1));
+        const int max_s = (items + floor_items - 1) / floor_items;
+        if (S > max_s) S = max_s;
     }
-    if (S > k_max) S = k_max;
+    if (S > items) S = items;
     if (S < 1) S = 1;
-    const int ips = (k_max + S - 1) / S;
-    return (k_max + ips - 1) / ips;
+    const int ips = (items + S - 1) / S;
+    return (items + ips - 1) / ips;
+}
+
+int sparse_splits(const spd_dims* d, int k_max, int req, int sms) {
+    const long long rows = (long long)d->B * d->H_kv;
+    const long long workers = (long long)sms * occ_sparse_attn(d->D, d->page_size);
+    return splits_for(rows, k_max, workers, pages_per_split_floor(d->page_size), 4, req);
 }
 
 int dense_splits(const spd_dims* d, int T, int req, int sms) {
-    const int P = d->max_pages_per_seq;
-    int S = req;
-    if (S <= 0) {
-        const long long rows = (long long)d->B * d->H_kv;
-        const int mt = attn_mtiles(T, d->H_q / d->H_kv);
-        const long long slots = (long long)sms * occ_dense_attn(d->D, d->page_size, mt);
-        const int floor_items = 2 * pages_per_split_floor(d->page_size);
-        S = 1;
-        while (rows * S < 4 * slots && (P + 2 * S - 1) / (2 * S) >= floor_items) S *= 2;
-    }
-    if (S > P) S = P;
-    if (S < 1) S = 1;
-    const int ips = (P + S - 1) / S;
-    return (P + ips - 1) / ips;
+    const long long rows = (long long)d->B * d->H_kv;
+    const int mt = attn_mtiles(T, d->H_q / d->H_kv);
+    const long long workers = (long long)sms * occ_dense_attn(d->D, d->page_size, mt);
+    return splits_for(rows, d->max_pages_per_seq, workers, 2 * pages_per_split_floor(d->page_size), 12, req);
 }
 
 struct AttnWs {
+    int* queue;
     int* counters;
     float* part_lse;
     float* part_o;
     size_t bytes;
 };
 
+// [queue: 16 B][row tickets][partial lse][partial o]; the first two must start zeroed.
 AttnWs attn_ws_layout(void* ws, long long rows, int S, int R, int D) {
     AttnWs w;
     size_t off = 0;
-    w.counters = reinterpret_cast<int*>(ws);
-    off += align256(rows * sizeof(int));
-    w.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + off);
+    char* base = static_cast<char*>(ws);
+    w.queue = reinterpret_cast<int*>(base);
+    off += 16;
+    w.counters = reinterpret_cast<int*>(base + off);
+    off = align256(off + rows * sizeof(int));
+    w.part_lse = reinterpret_cast<float*>(base + off);
     off += align256((size_t)rows * S * R * sizeof(float));
-    w.part_o = reinterpret_cast<float*>(static_cast<char*>(ws) + off);
+    w.part_o = reinterpret_cast<float*>(base + off);
     off += (size_t)rows * S * R * D * sizeof(float);
     w.bytes = off;
     return w;
@@ -294,6 +295,7 @@ SPD_API spd_status pages_score_select(const spd_dims* dims, const spd_bf16* q, c
     if (!aligned16(q) || !aligned16(summ)) return fail(SPD_ERR_INVALID_ARG, "q and summ must be 16-byte aligned");
     const size_t need = spd_score_select_workspace_size(dims);
     if (!ws || ws_bytes < need) return fail(SPD_ERR_WORKSPACE, "workspace %zu bytes < %zu", ws_bytes, need);
+    if (!aligned16(ws)) return fail(SPD_ERR_INVALID_ARG, "ws must be 16-byte aligned");
     DevInfo* d = dev_info(&st);
     if (!d) return st;
     const long long rows = (long long)dims->B * dims->H_kv;
@@ -349,6 +351,7 @@ SPD_API spd_status sparse_decode_attn(const spd_dims* dims, const spd_bf16* q, c
     const long long rows = (long long)dims->B * dims->H_kv;
     AttnWs w = attn_ws_layout(ws, rows, S, G, dims->D);
     if (!ws || ws_bytes < w.bytes) return fail(SPD_ERR_WORKSPACE, "workspace %zu bytes < %zu", ws_bytes, w.bytes);
+    if (!aligned16(ws)) return fail(SPD_ERR_INVALID_ARG, "ws must be 16-byte aligned");
     CUtensorMap tk, tv;
     if ((st = kv_map(&tk, K, dims)) != SPD_OK || (st = kv_map(&tv, V, dims)) != SPD_OK) return st;
     AttnArgs a;
@@ -374,6 +377,8 @@ SPD_API spd_status sparse_decode_attn(const spd_dims* dims, const spd_bf16* q, c
     a.part_o = w.part_o;
     a.part_lse = w.part_lse;
     a.counters = w.counters;
+    a.queue = w.queue;
+    a.num_sms = d->sms;
     a.status = d->status;
     cudaError_t e = launch_sparse_attn(a, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SPD_OK : cuda_fail(e, "sparse_decode_attn launch");
@@ -396,6 +401,7 @@ SPD_API spd_status dense_verify_attn(const spd_dims* dims, int32_t T, const spd_
     const long long rows = (long long)dims->B * dims->H_kv;
     AttnWs w = attn_ws_layout(ws, rows, S, T * G, dims->D);
     if (!ws || ws_bytes < w.bytes) return fail(SPD_ERR_WORKSPACE, "workspace %zu bytes < %zu", ws_bytes, w.bytes);
+    if (!aligned16(ws)) return fail(SPD_ERR_INVALID_ARG, "ws must be 16-byte aligned");
     CUtensorMap tk, tv;
     if ((st = kv_map(&tk, K, dims)) != SPD_OK || (st = kv_map(&tv, V, dims)) != SPD_OK) return st;
     AttnArgs a;
@@ -421,6 +427,8 @@ SPD_API spd_status dense_verify_attn(const spd_dims* dims, int32_t T, const spd_
     a.part_o = w.part_o;
     a.part_lse = w.part_lse;
     a.counters = w.counters;
+    a.queue = w.queue;
+    a.num_sms = d->sms;
     a.status = d->status;
     cudaError_t e = launch_dense_attn(a, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SPD_OK : cuda_fail(e, "dense_verify_attn launch");
