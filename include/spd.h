@@ -189,6 +189,40 @@ spd_status sparse_decode_attn(const spd_dims *dims, const spd_bf16 *q, const spd
                               spd_bf16 *o, float *lse, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * sparse_decode_attn_noalloc -- sparse_decode_attn for callers that cannot
+ * allocate device memory.  It has no counterpart on the pages: it is the same
+ * computation, with the same arguments and results as sparse_decode_attn,
+ * minus the workspace.
+ *
+ * Who needs it: code that runs where a cudaMalloc is not allowed or not
+ * wanted -- an inference engine that owns all device memory through a fixed
+ * arena and gives plug-ins no workspace argument, or a latency-critical decode
+ * loop that must not call cudaMalloc because it can synchronise the device
+ * and stall every stream.  Such a caller still passes q, K, V, the page table,
+ * the selection and the outputs; the scratch this call needs (the unit queue,
+ * the split tickets and the split partials) lives in a fixed array compiled
+ * into the library, SPD_NOALLOC_SCRATCH_BYTES (8 MiB) per GPU, which every GPU
+ * that loads the library holds until the process exits.
+ *
+ * Behaviour: the first call on a device looks up that array's device address
+ * (once per device, with that device current); make that first call before
+ * any stream capture.  Each call clears the array's counters on `stream`
+ * (cudaMemsetAsync) and never calls cudaMalloc, cudaFree or any allocating
+ * library routine.  The split count is num_splits, or with num_splits = 0 the
+ * automatic count lowered until the partials fit the array; if the requested
+ * split count (or even one split) needs more scratch than the array holds, the
+ * call returns SPD_ERR_UNSUPPORTED and launches nothing.  All calls share the
+ * one array: calls that overlap on the GPU (different streams, or different
+ * host threads without ordering) race and give wrong results.
+ */
+#define SPD_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+spd_status sparse_decode_attn_noalloc(const spd_dims *dims, const spd_bf16 *q, const spd_bf16 *K,
+                                      const spd_bf16 *V, const int32_t *page_table,
+                                      const int32_t *seq_lens, const int32_t *sel,
+                                      const int32_t *nsel, int32_t k_max, int32_t num_splits,
+                                      float softmax_scale, spd_bf16 *o, float *lse, void *stream);
+
+/*
  * dense_verify_attn -- dense causal verification of T drafted positions over
  * the complete KV cache (S3R abstract; Table 7 "Verify (TV)", k = 6 so T = 7).
  *

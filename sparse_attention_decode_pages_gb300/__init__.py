@@ -19,6 +19,7 @@ import os
 __all__ = [
     "SpdError", "Dims", "Policy", "lib", "dims_of", "policy_of", "workspace",
     "pages_summarize", "pages_score_select", "sparse_decode_attn", "dense_verify_attn",
+    "sparse_decode_attn_noalloc",
     "lse_merge", "spd_device_status", "spd_score_select_workspace_size",
     "spd_sparse_decode_workspace_size", "spd_dense_verify_workspace_size",
     "DEV_BAD_PAGE", "DEV_BAD_SEL", "DEV_TIMEOUT",
@@ -79,9 +80,12 @@ def lib():
         L.sparse_decode_attn.argtypes = [DP, P, P, P, P, P, P, P, i32, i32, ctypes.c_float,
                                          P, P, P, sz, P]
         L.dense_verify_attn.argtypes = [DP, i32, P, P, P, P, P, i32, ctypes.c_float, P, P, P, sz, P]
+        L.sparse_decode_attn_noalloc.argtypes = [DP, P, P, P, P, P, P, P, i32, i32, ctypes.c_float,
+                                                 P, P, P]
         L.lse_merge.argtypes = [i32, i32, i32, P, P, P, P, P]
         for f in ("spd_device_status", "pages_summarize", "pages_score_select",
-                  "sparse_decode_attn", "dense_verify_attn", "lse_merge"):
+                  "sparse_decode_attn", "dense_verify_attn", "lse_merge",
+                  "sparse_decode_attn_noalloc"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -173,6 +177,17 @@ def sparse_decode_attn(dims: Dims, q, K, V, page_table, seq_lens, sel, nsel, k_m
                                     _ptr(seq_lens), _ptr(sel), _ptr(nsel), k_max, num_splits,
                                     scale, _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
                                     _stream(stream)))
+
+
+def sparse_decode_attn_noalloc(dims: Dims, q, K, V, page_table, seq_lens, sel, nsel, k_max: int, o,
+                               lse=None, num_splits: int = 0, softmax_scale: float | None = None,
+                               stream=None):
+    """sparse_decode_attn without a workspace: its scratch is a fixed array inside the library."""
+    scale = 1.0 / math.sqrt(dims.D) if softmax_scale is None else softmax_scale
+    _check(lib().sparse_decode_attn_noalloc(ctypes.byref(dims), _ptr(q), _ptr(K), _ptr(V),
+                                            _ptr(page_table), _ptr(seq_lens), _ptr(sel), _ptr(nsel),
+                                            k_max, num_splits, scale, _ptr(o), _ptr(lse),
+                                            _stream(stream)))
 
 
 def dense_verify_attn(dims: Dims, T: int, q, K, V, page_table, seq_lens, o, ws, lse=None,

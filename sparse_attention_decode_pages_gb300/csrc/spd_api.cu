@@ -443,3 +443,111 @@ SPD_API spd_status lse_merge(int32_t S, int32_t rows, int32_t D, const float* pa
     cudaError_t e = launch_lse_merge(S, rows, D, part_o, part_lse, o, lse, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SPD_OK : cuda_fail(e, "lse_merge launch");
 }
+
+// ---------------------------------------------------------------------------
+// sparse_decode_attn_noalloc: the same launch with its scratch in a fixed
+// device array instead of a caller workspace (see include/spd.h).
+
+namespace spd {
+namespace {
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[SPD_NOALLOC_SCRATCH_BYTES];
+
+struct NoAllocDev {
+    std::once_flag once;
+    void* ptr = nullptr;
+    cudaError_t err = cudaSuccess;
+};
+NoAllocDev g_noalloc[kMaxDevices];
+
+// Device address of the fixed scratch array for the current device (looked up
+// once per device; in host code the array's name is only a host-side handle).
+void* noalloc_scratch(spd_status* st) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *st = cuda_fail(e, "cudaGetDevice");
+        return nullptr;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        *st = fail(SPD_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+        return nullptr;
+    }
+    NoAllocDev* n = &g_noalloc[dev];
+    std::call_once(n->once, [n]() { n->err = cudaGetSymbolAddress(&n->ptr, g_noalloc_scratch); });
+    if (n->err != cudaSuccess || !n->ptr) {
+        *st = cuda_fail(n->err, "looking up the fixed scratch array");
+        return nullptr;
+    }
+    return n->ptr;
+}
+
+}  // namespace
+}  // namespace spd
+
+SPD_API spd_status sparse_decode_attn_noalloc(const spd_dims* dims, const spd_bf16* q, const spd_bf16* K,
+                                              const spd_bf16* V, const int32_t* page_table, const int32_t* seq_lens,
+                                              const int32_t* sel, const int32_t* nsel, int32_t k_max,
+                                              int32_t num_splits, float softmax_scale, spd_bf16* o, float* lse,
+                                              void* stream) {
+    spd_status st = check_dims(dims);
+    if (st != SPD_OK) return st;
+    if (k_max < 1) return fail(SPD_ERR_INVALID_ARG, "k_max < 1");
+    if (num_splits < 0) return fail(SPD_ERR_INVALID_ARG, "num_splits < 0");
+    if (dims->B == 0) return SPD_OK;
+    if ((st = attn_common(dims, q, K, V, page_table, seq_lens, o)) != SPD_OK) return st;
+    if (!sel || !nsel) return fail(SPD_ERR_INVALID_ARG, "NULL selection");
+    DevInfo* d = dev_info(&st);
+    if (!d) return st;
+    void* scratch = noalloc_scratch(&st);
+    if (!scratch) return st;
+    const int G = dims->H_q / dims->H_kv;
+    const long long rows = (long long)dims->B * dims->H_kv;
+    int S = sparse_splits(dims, k_max, num_splits, d->sms);
+    AttnWs w = attn_ws_layout(scratch, rows, S, G, dims->D);
+    if (num_splits == 0) {
+        // automatic: the largest split count up to the usual one whose partials fit
+        while (w.bytes > SPD_NOALLOC_SCRATCH_BYTES && S > 1) {
+            S = sparse_splits(dims, k_max, S - 1, d->sms);
+            w = attn_ws_layout(scratch, rows, S, G, dims->D);
+        }
+    }
+    if (w.bytes > SPD_NOALLOC_SCRATCH_BYTES)
+        return fail(SPD_ERR_UNSUPPORTED,
+                    "sparse_decode_attn_noalloc needs %zu bytes of scratch for %d split(s); the fixed array holds %zu",
+                    w.bytes, S, (size_t)SPD_NOALLOC_SCRATCH_BYTES);
+    CUtensorMap tk, tv;
+    if ((st = kv_map(&tk, K, dims)) != SPD_OK || (st = kv_map(&tv, V, dims)) != SPD_OK) return st;
+    // the queue and the split tickets must start at zero
+    const size_t zero_bytes = reinterpret_cast<char*>(w.part_lse) - static_cast<char*>(scratch);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, zero_bytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the fixed scratch array");
+    AttnArgs a;
+    a.q = q;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.sel = sel;
+    a.nsel = nsel;
+    a.k_max = k_max;
+    a.B = dims->B;
+    a.H_q = dims->H_q;
+    a.H_kv = dims->H_kv;
+    a.D = dims->D;
+    a.ps = dims->page_size;
+    a.max_pages = dims->max_pages_per_seq;
+    a.T = 1;
+    a.num_phys = dims->num_phys_pages;
+    a.items_per_split = (k_max + S - 1) / S;
+    a.num_splits = S;
+    a.scale_log2 = softmax_scale * kLog2e;
+    a.o = o;
+    a.lse = lse;
+    a.part_o = w.part_o;
+    a.part_lse = w.part_lse;
+    a.counters = w.counters;
+    a.queue = w.queue;
+    a.num_sms = d->sms;
+    a.status = d->status;
+    e = launch_sparse_attn(a, tk, tv, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPD_OK : cuda_fail(e, "sparse_decode_attn_noalloc launch");
+}
