@@ -170,7 +170,7 @@ def run_gpu(args):
         w.q_verify = wl.f32_to_bf16_bits(rng.standard_normal((w.B, T, w.H_q, w.D)).astype(np.float32))
     d = wl.to_device(w, dev)
     dims = spd.dims_of(w.B, w.H_q, w.H_kv, w.D, w.page_size, w.max_pages_per_seq, w.num_phys_pages)
-    summ = torch.empty((w.num_phys_pages, w.H_kv, 2, w.D), dtype=torch.bfloat16, device=dev)
+    summ = torch.empty((w.B, w.H_kv, w.max_pages_per_seq, 2, w.D), dtype=torch.bfloat16, device=dev)
     spd.pages_summarize(dims, d["K"], d["page_table"], d["seq_lens"], summ)  # prefill
     last = torch.tensor([b * w.max_pages_per_seq + (int(w.seq_lens[b]) - 1) // w.page_size
                          for b in range(w.B)], dtype=torch.int32, device=dev)
@@ -194,7 +194,7 @@ def run_gpu(args):
         spd.pages_summarize(dims, d["K"], d["page_table"], d["seq_lens"], summ, only_pages=last)
         if ev:
             ev[1].record(stream)
-        spd.pages_score_select(dims, d["q"], summ, d["page_table"], d["seq_lens"], policy, sel,
+        spd.pages_score_select(dims, d["q"], summ, d["seq_lens"], policy, sel,
                                nsel, k_max, ws_sel)
         if ev:
             ev[2].record(stream)

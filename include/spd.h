@@ -132,10 +132,13 @@ size_t spd_dense_verify_workspace_size(const spd_dims *dims, int32_t T, int32_t 
  * scoring rule reads; the pages' cost model charges one scoring read per
  * generated page: Sparrow, "Control Study 2", scoring term).
  *
- * For each listed page and each KV head h, writes the channel-wise minimum and
- * maximum of the keys of the page's valid tokens (positions < seq_lens[b]):
- *   summ[phys][h][0][d] = min_t K[phys][h][t][d],  summ[phys][h][1][d] = max_t ...
- * summ is bf16 [num_phys_pages][H_kv][2][D]; bf16 min/max is exact.
+ * For each listed (sequence b, logical page p) and each KV head h, writes the
+ * channel-wise minimum and maximum of the keys of the page's valid tokens
+ * (positions < seq_lens[b]), phys = page_table[b][p]:
+ *   summ[b][h][p][0][d] = min_t K[phys][h][t][d],  summ[b][h][p][1][d] = max_t ...
+ * summ is bf16 [B][H_kv][max_pages_per_seq][2][D], sequence-major so that
+ * scoring a (sequence, KV head) row reads one contiguous stream; bf16 min/max
+ * is exact.
  * only_pages: NULL = every logical page of every sequence; otherwise n_only
  * entries, each b * max_pages_per_seq + p (a slot of page_table), e.g. the
  * page the newest token was written to.  Entries whose p is past the
@@ -150,8 +153,9 @@ spd_status pages_summarize(const spd_dims *dims, const spd_bf16 *K, const int32_
  * (Sparrow, "Control Study 2": KV budget B, page size, Top-k over pages;
  * "Control Study 1": length-scheduled budget).
  *
- * q is bf16 [B][H_q][D] (the decode query).  For every sequence b, KV head h
- * and page p < P_b, the score is
+ * q is bf16 [B][H_q][D] (the decode query); summ is the [B][H_kv][max_pages][2][D]
+ * array pages_summarize maintains.  For every sequence b, KV head h and page
+ * p < P_b, the score is
  *   score(p) = max_{g < G} sum_d max(q[b][hG+g][d] * kmin[d], q[b][hG+g][d] * kmax[d])
  * (an upper bound of q.k over the page's keys), accumulated in fp32 from the
  * bf16 summaries.  Then the mandatory pages plus the best-scoring remaining
@@ -164,7 +168,7 @@ spd_status pages_summarize(const spd_dims *dims, const spd_bf16 *K, const int32_
  * Requires k_max >= sink_pages + local_pages.
  */
 spd_status pages_score_select(const spd_dims *dims, const spd_bf16 *q, const spd_bf16 *summ,
-                              const int32_t *page_table, const int32_t *seq_lens,
+                              const int32_t *seq_lens,
                               const spd_budget_policy *policy, int32_t *sel, int32_t *nsel,
                               int32_t k_max, float *scores, void *ws, size_t ws_bytes,
                               void *stream);

@@ -76,7 +76,7 @@ def lib():
         L.spd_dense_verify_workspace_size.argtypes = [DP, i32, i32]
         L.spd_dense_verify_workspace_size.restype = sz
         L.pages_summarize.argtypes = [DP, P, P, P, P, i32, P, P]
-        L.pages_score_select.argtypes = [DP, P, P, P, P, PP, P, P, i32, P, P, sz, P]
+        L.pages_score_select.argtypes = [DP, P, P, P, PP, P, P, i32, P, P, sz, P]
         L.sparse_decode_attn.argtypes = [DP, P, P, P, P, P, P, P, i32, i32, ctypes.c_float,
                                          P, P, P, sz, P]
         L.dense_verify_attn.argtypes = [DP, i32, P, P, P, P, P, i32, ctypes.c_float, P, P, P, sz, P]
@@ -161,11 +161,11 @@ def pages_summarize(dims: Dims, K, page_table, seq_lens, summ, only_pages=None, 
                                  _ptr(only_pages), n_only, _ptr(summ), _stream(stream)))
 
 
-def pages_score_select(dims: Dims, q, summ, page_table, seq_lens, policy, sel, nsel, k_max: int,
-                       ws, scores=None, stream=None):
+def pages_score_select(dims: Dims, q, summ, seq_lens, policy, sel, nsel, k_max: int, ws,
+                       scores=None, stream=None):
     pol = policy if isinstance(policy, Policy) else policy_of(policy)
-    _check(lib().pages_score_select(ctypes.byref(dims), _ptr(q), _ptr(summ), _ptr(page_table),
-                                    _ptr(seq_lens), ctypes.byref(pol), _ptr(sel), _ptr(nsel), k_max,
+    _check(lib().pages_score_select(ctypes.byref(dims), _ptr(q), _ptr(summ), _ptr(seq_lens),
+                                    ctypes.byref(pol), _ptr(sel), _ptr(nsel), k_max,
                                     _ptr(scores), _ptr(ws), ws.numel(), _stream(stream)))
 
 

@@ -25,8 +25,7 @@ cudaError_t launch_summarize(const SummarizeArgs& a, cudaStream_t st);
 
 struct ScoreSelectArgs {
     const uint16_t* q;
-    const uint16_t* summ;
-    const int32_t* page_table;
+    const uint16_t* summ;  // [B][H_kv][max_pages][2][D]
     const int32_t* seq_lens;
     spd_budget_policy pol;
     int32_t* sel;
@@ -38,10 +37,8 @@ struct ScoreSelectArgs {
     long long num_phys;
     unsigned* status;
 };
-// Pages scored per CTA (a multiple of 64), and the dynamic shared memory the
-// selection needs.
-int score_chunk_pages(int max_pages, int rows, int num_sms);
-cudaError_t launch_score_select(const ScoreSelectArgs& a, int chunk_pages, cudaStream_t st);
+// Scores every page (persistent grid sized to num_sms), then selects per row.
+cudaError_t launch_score_select(const ScoreSelectArgs& a, int num_sms, cudaStream_t st);
 
 struct AttnArgs {
     const uint16_t* q;  // [B][T][H_q][D] (T = 1 for decode)

@@ -11,21 +11,23 @@
 // query heads form one m16n8 MMA tile per 16 summary channels.  The bf16
 // products are exact in fp32; accumulation is fp32.
 //
-// Work layout: grid (chunks, H_kv, B); a CTA of 4 warps scores one chunk of
-// pages of one (sequence, KV head).  Every warp owns a ring of shared-memory
-// slots, one 16-page tile each, filled by 1-D bulk copies (one 512-byte
-// summary per lane, completion counted on the slot's mbarrier) several tiles
-// ahead of the MMAs.  Pages sit at a padded stride so that the 16-byte
-// fragment reads of a quarter-warp hit distinct banks.  The summary channels
-// are assigned to MMA k-slots in the order each thread reads them and the
-// query operand uses the same order (the contraction is a sum, so any common
-// order is exact), so no shuffles or ldmatrix are needed.
+// Work layout: a persistent grid (two CTAs of 4 warps per SM).  All 16-page
+// tiles of all (sequence, KV head) rows are numbered in one sequence and every
+// warp takes an equal contiguous share, so the work is balanced to a tile.
+// The summaries are stored sequence-major, so a tile is one contiguous 8 KB
+// run: every warp owns a ring of shared-memory slots filled by one 1-D bulk
+// copy per tile (completion counted on the slot's mbarrier) several tiles
+// ahead of the MMAs.  The summary channels are assigned to MMA
+// k-slots in the order each thread reads them and the query operand uses the
+// same order (the contraction is a sum, so any common order is exact), so no
+// shuffles or ldmatrix are needed.
 //
-// Selection: the last CTA to finish a row (an atomic ticket; nothing waits)
-// selects that row's pages: the mandatory pages, then the k'-th best score is
-// found by bisection over order-preserving uint32 keys (32 counting rounds,
-// one barrier each), and pages above it plus the lowest-id pages equal to it
-// are compacted in ascending order into sel[].
+// Selection (a second kernel, one warp per (sequence, KV head) row): the
+// mandatory pages, then the k'-th best score by an 8-bit radix select over
+// order-preserving uint32 keys (4 passes; shared-memory histogram with
+// warp-aggregated atomics, since neighbouring scores share their high bytes),
+// and pages above it plus the lowest-id pages equal to it, compacted in
+// ascending order into sel[] with ballots.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -38,33 +40,10 @@ constexpr int kScoreStages = 3;
 template <int D>
 struct ScoreCfg {
     static constexpr int PAGE_BYTES = 2 * D * 2;      // [kmin | kmax] bf16
-    static constexpr int STRIDE = PAGE_BYTES + 64;    // consecutive pages 16 banks apart
-    static constexpr int TILE = 16 * STRIDE;
+    static constexpr int TILE = 16 * PAGE_BYTES;
     static constexpr int RING = kScoreWarps * kScoreStages * TILE;
     static constexpr int BARS = kScoreWarps * kScoreStages * 8;
 };
-
-// Exclusive prefix sum over the CTA; returns this thread's prefix and the total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, x, off);
-        if (lane >= off) x += y;
-    }
-    if (lane == 31) warp_tot[warp] = x;
-    __syncthreads();
-    int base = 0, tot = 0;
-#pragma unroll
-    for (int w = 0; w < kScoreWarps; ++w) {
-        if (w < warp) base += warp_tot[w];
-        tot += warp_tot[w];
-    }
-    __syncthreads();
-    total = tot;
-    return base + x - v;
-}
 
 __device__ __forceinline__ long long budget_pages(const spd_budget_policy& pol, long long len,
                                                   long long ps) {
@@ -77,39 +56,52 @@ __device__ __forceinline__ long long budget_pages(const spd_budget_policy& pol, 
     return (len * pol.frac_num + pol.frac_den * ps - 1) / (pol.frac_den * ps);
 }
 
-// CTA-wide count of non-mandatory keys satisfying `pred`, one barrier.
-template <typename Pred>
-__device__ __forceinline__ int count_keys(const uint32_t* keys, int P, int sink, int local, Pred pred,
-                                          int (*red)[kScoreWarps], int buf) {
-    int cnt = 0;
-    for (int p = threadIdx.x; p < P; p += kScoreThreads)
-        if (!(p < sink || p >= P - local) && pred(keys[p])) ++cnt;
-    cnt = __reduce_add_sync(0xffffffffu, cnt);
-    if ((threadIdx.x & 31) == 0) red[buf][threadIdx.x >> 5] = cnt;
-    __syncthreads();
-    int tot = 0;
-#pragma unroll
-    for (int w = 0; w < kScoreWarps; ++w) tot += red[buf][w];
-    return tot;
-}
+constexpr int kSelWarps = 8;
+constexpr int kSelThreads = 32 * kSelWarps;
 
-// Selection for one (sequence, KV head) row by the CTA that finished it last.
-__device__ void select_row(const ScoreSelectArgs& a, int b, int h, int P, int len, uint32_t* keys) {
-    __shared__ int warp_tot[kScoreWarps];
-    __shared__ int red[2][kScoreWarps];
-    const int tid = threadIdx.x;
+// Selection of one (sequence, KV head) row by a CTA of 8 warps.  keys holds
+// the row's order-preserving score keys in shared memory.
+__global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) {
+    extern __shared__ uint32_t keys[];
+    __shared__ uint32_t hist[256];
+    __shared__ int s_digit, s_rem;
+    __shared__ int w_eq[kSelWarps], w_take[kSelWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    const int row = blockIdx.x;
+    const int b = row / a.H_kv;
+    const int len = a.seq_lens[b];
+    const int P = (len + a.ps - 1) / a.ps;
+    int32_t* out = a.sel + (long long)row * a.k_max;
+    if (P <= 0) {
+        if (tid == 0) a.nsel[row] = 0;
+        return;
+    }
     const int sink = min(a.pol.sink_pages, P), local = min(a.pol.local_pages, P);
     const int nm = min(P, sink + local);
     long long k = budget_pages(a.pol, len, a.ps);
     if (k > a.k_max) k = a.k_max;
     if (k < nm) k = nm;
     if (k > P) k = P;
-    const int kp = (int)k - nm;   // pages to pick among the non-mandatory ones
+    const int kp = (int)k - nm;  // pages to pick among the non-mandatory ones
     const int ncand = P - nm;
     auto mand = [&](int p) { return p < sink || p >= P - local; };
 
-    const float* sc = a.scores + ((long long)b * a.H_kv + h) * a.max_pages;
-    for (int p = tid; p < P; p += kScoreThreads) keys[p] = float_key(__ldcg(sc + p));
+    // keys: each thread's loads are independent and issued back to back
+    const float* sc = a.scores + (long long)row * a.max_pages;
+    for (int p0 = 0; p0 < P; p0 += kSelThreads * 4) {
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int p = p0 + i * kSelThreads + tid;
+            v[i] = p < P ? sc[p] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int p = p0 + i * kSelThreads + tid;
+            if (p < P) keys[p] = float_key(v[i]);
+        }
+    }
     __syncthreads();
 
     uint32_t thr;
@@ -121,237 +113,317 @@ __device__ void select_row(const ScoreSelectArgs& a, int b, int h, int P, int le
         thr = 0u;
         rem = ncand;
     } else {
-        // Largest T with #{key >= T} >= kp: the kp-th largest key.
-        uint32_t T = 0;
-        int buf = 0;
-        for (int bit = 31; bit >= 0; --bit) {
-            const uint32_t cand = T | (1u << bit);
-            const int c = count_keys(keys, P, sink, local, [cand](uint32_t u) { return u >= cand; }, red, buf);
-            buf ^= 1;
-            if (c >= kp) T = cand;
+        uint32_t prefix = 0, pmask = 0;
+        rem = kp;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            hist[tid] = 0;  // kSelThreads == 256 bins
+            __syncthreads();
+            for (int p0 = 0; p0 < P; p0 += kSelThreads) {
+                const int p = p0 + tid;
+                bool in = false;
+                uint32_t bin = 0;
+                if (p < P && !mand(p)) {
+                    const uint32_t u = keys[p];
+                    in = (u & pmask) == prefix;
+                    bin = (u >> shift) & 255u;
+                }
+                const unsigned act = __ballot_sync(0xffffffffu, in);
+                if (in) {  // neighbouring scores share bins: one atomic per distinct bin
+                    const unsigned same = __match_any_sync(act, bin);
+                    if (lane == __ffs(same) - 1) atomicAdd(hist + bin, (uint32_t)__popc(same));
+                }
+            }
+            __syncthreads();
+            if (warp == 0) {
+                // lane l owns bins 255-8l .. 248-8l, visited from the top
+                uint32_t cnt[8];
+                int sum = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    cnt[i] = hist[255 - 8 * lane - i];
+                    sum += (int)cnt[i];
+                }
+                int incl = sum;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += y;
+                }
+                const int excl = incl - sum;
+                const unsigned hit = __ballot_sync(0xffffffffu, excl < rem && rem <= incl);
+                if (lane == __ffs(hit) - 1) {
+                    int cum = excl;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (cum + (int)cnt[i] >= rem) {
+                            s_digit = 255 - 8 * lane - i;
+                            s_rem = rem - cum;
+                            break;
+                        }
+                        cum += (int)cnt[i];
+                    }
+                }
+            }
+            __syncthreads();
+            prefix |= (uint32_t)s_digit << shift;
+            pmask |= 255u << shift;
+            rem = s_rem;
         }
-        const int gt = count_keys(keys, P, sink, local, [T](uint32_t u) { return u > T; }, red, buf);
-        thr = T;
-        rem = kp - gt;
+        thr = prefix;
     }
 
     // Ascending compaction: mandatory pages, keys above the threshold, and the
-    // first `rem` keys equal to it in page order.
-    const int seg = (P + kScoreThreads - 1) / kScoreThreads;
-    const int lo = min(P, tid * seg), hi = min(P, lo + seg);
+    // first `rem` keys equal to it in page order.  Warp w owns a contiguous
+    // segment of pages; per-warp counts are scanned through shared memory.
+    const int seg = ((P + kSelWarps * 32 - 1) / (kSelWarps * 32)) * 32;
+    const int lo = min(P, warp * seg), hi = min(P, lo + seg);
     int n_eq = 0;
-    for (int p = lo; p < hi; ++p)
-        if (!mand(p) && keys[p] == thr) ++n_eq;
-    int total;
-    const int eq_base = block_exclusive_scan(n_eq, warp_tot, total);
+    for (int p0 = lo; p0 < hi; p0 += 32) {
+        const int p = p0 + lane;
+        n_eq += __popc(__ballot_sync(0xffffffffu, p < hi && !mand(p) && keys[p] == thr));
+    }
+    if (lane == 0) w_eq[warp] = n_eq;
+    __syncthreads();
+    int eq_before = 0;
+    for (int w = 0; w < warp; ++w) eq_before += w_eq[w];
     int n_take = 0;
     {
-        int eq = eq_base;
-        for (int p = lo; p < hi; ++p) {
-            bool take = mand(p);
-            if (!take) {
-                const uint32_t u = keys[p];
-                if (u == thr) take = (eq++ < rem);
-                else take = u > thr;
+        int eqb = eq_before;
+        for (int p0 = lo; p0 < hi; p0 += 32) {
+            const int p = p0 + lane;
+            bool m = false, eq = false, gt = false;
+            if (p < hi) {
+                m = mand(p);
+                if (!m) {
+                    const uint32_t u = keys[p];
+                    eq = u == thr;
+                    gt = u > thr;
+                }
             }
-            n_take += take;
+            const unsigned eb = __ballot_sync(0xffffffffu, eq);
+            const bool take = m || gt || (eq && eqb + __popc(eb & lt_mask) < rem);
+            n_take += __popc(__ballot_sync(0xffffffffu, take));
+            eqb += __popc(eb);
         }
     }
-    const int out_base = block_exclusive_scan(n_take, warp_tot, total);
-    int32_t* out = a.sel + ((long long)b * a.H_kv + h) * a.k_max;
+    if (lane == 0) w_take[warp] = n_take;
+    __syncthreads();
+    int pos = 0, total = 0;
+    for (int w = 0; w < kSelWarps; ++w) {
+        if (w < warp) pos += w_take[w];
+        total += w_take[w];
+    }
     {
-        int eq = eq_base, pos = out_base;
-        for (int p = lo; p < hi; ++p) {
-            bool take = mand(p);
-            if (!take) {
-                const uint32_t u = keys[p];
-                if (u == thr) take = (eq++ < rem);
-                else take = u > thr;
+        int eqb = eq_before;
+        for (int p0 = lo; p0 < hi; p0 += 32) {
+            const int p = p0 + lane;
+            bool m = false, eq = false, gt = false;
+            if (p < hi) {
+                m = mand(p);
+                if (!m) {
+                    const uint32_t u = keys[p];
+                    eq = u == thr;
+                    gt = u > thr;
+                }
             }
-            if (take) {
-                if (pos < a.k_max) out[pos] = p;
-                ++pos;
-            }
+            const unsigned eb = __ballot_sync(0xffffffffu, eq);
+            const bool take = m || gt || (eq && eqb + __popc(eb & lt_mask) < rem);
+            const unsigned tb = __ballot_sync(0xffffffffu, take);
+            const int at = pos + __popc(tb & lt_mask);
+            if (take && at < a.k_max) out[at] = p;
+            pos += __popc(tb);
+            eqb += __popc(eb);
         }
     }
     if (tid == 0) {
         if (total > a.k_max) raise_status(a.status, SPD_DEV_BAD_SEL);
-        a.nsel[(long long)b * a.H_kv + h] = min(total, a.k_max);
+        a.nsel[row] = min(total, a.k_max);
     }
 }
 
 template <int D>
-__global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelectArgs a, int chunk_pages) {
+__global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelectArgs a, int unused) {
     using C = ScoreCfg<D>;
-    constexpr int NSS = 2 * D / 32;  // 32-channel super-steps over [kmin | kmax]
+    constexpr int NSS = 2 * D / 32;   // 32-channel super-steps over [kmin | kmax]
+    constexpr int SLOT = C::TILE;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ int s_last;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-
-    const int b = blockIdx.z, h = blockIdx.y, chunk = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int len = a.seq_lens[b];
-    const int P = (len + a.ps - 1) / a.ps;
-    const int nch = (P + chunk_pages - 1) / chunk_pages;
-    if (chunk >= nch) {
-        if (chunk == 0 && threadIdx.x == 0) a.nsel[(long long)b * a.H_kv + h] = 0;
-        return;
-    }
     const int G = a.H_q / a.H_kv;
     const int n = lane >> 2, c = lane & 3;  // B operand: query head n of the group, k-slot group c
 
-    const int32_t* pt = a.page_table + (long long)b * a.max_pages;
-    const int chunk_lo = chunk * chunk_pages;
-    const int chunk_hi = min(P, chunk_lo + chunk_pages);
-    // this warp's tiles: p0 = chunk_lo + (warp + 4 t) * 16
-    const int span = chunk_hi - chunk_lo;
-    const int ntiles_all = (span + 15) / 16;
-    const int ntile = ntiles_all > warp ? (ntiles_all - warp + kScoreWarps - 1) / kScoreWarps : 0;
-
-    // [barriers (128 B)][this chunk's page ids][ring: warps x stages x tiles];
-    // the selection keys reuse the ring.
-    int* s_pt = reinterpret_cast<int*>(smem + 128);
-    uint8_t* ring_base = smem + 128 + ((chunk_pages * 4 + 127) & ~127);
-    uint8_t* ring = ring_base + warp * kScoreStages * C::TILE;
+    // [barriers (128 B)][ring: warps x stages x tiles][tile prefix: B + 1 ints][pages: B ints]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem) + warp * kScoreStages;
+    uint8_t* ring = smem + 128 + warp * kScoreStages * SLOT;
+    int* pref = reinterpret_cast<int*>(smem + 128 + kScoreWarps * kScoreStages * SLOT);
+    int* pages = pref + a.B + 1;
     if (lane == 0) {
         for (int i = 0; i < kScoreStages; ++i) mbar_init(bars + i, 1);
         mbar_fence_init();
     }
-    for (int i = threadIdx.x; i < span; i += kScoreThreads) s_pt[i] = pt[chunk_lo + i];
+    // pref[b] = H_kv * (16-page tiles of sequences 0..b-1); a sequence's tiles are
+    // ordered (KV head, tile).
+    for (int bb = threadIdx.x; bb < a.B; bb += kScoreThreads) pages[bb] = (a.seq_lens[bb] + a.ps - 1) / a.ps;
     __syncthreads();
-
-    const uint16_t* summ_h = a.summ + (long long)h * 2 * D;
-    // Issue tile t into its slot: lanes 0..15 copy one page each.  Returns the
-    // mask of pages with a valid physical id.
-    auto issue = [&](int t) -> unsigned {
-        const int slot = t % kScoreStages;
-        const int p = chunk_lo + (warp + kScoreWarps * t) * 16 + lane;
-        bool ok = false;
-        long long phys = 0;
-        if (lane < 16 && p < chunk_hi) {
-            phys = s_pt[p - chunk_lo];
-            ok = phys >= 0 && phys < a.num_phys;
-            if (!ok) raise_status(a.status, SPD_DEV_BAD_PAGE);
-        }
-        const unsigned vm = __ballot_sync(0xffffffffu, ok);
-        if (lane == 0) mbar_arrive_expect_tx(bars + slot, __popc(vm) * C::PAGE_BYTES);
-        if (ok)
-            bulk_load(ring + slot * C::TILE + lane * C::STRIDE, summ_h + phys * a.H_kv * 2 * D, C::PAGE_BYTES,
-                      bars + slot);
-        return vm;
-    };
-    unsigned vmask[kScoreStages];
+    if (warp == 0) {
+        int run = 0;
+        for (int b0 = 0; b0 < a.B; b0 += 32) {
+            const int bb = b0 + lane;
+            const int t = bb < a.B ? (pages[bb] + 15) / 16 * a.H_kv : 0;
+            int incl = t;
 #pragma unroll
-    for (int i = 0; i < kScoreStages; ++i) vmask[i] = (i < ntile) ? issue(i) : 0u;
-
-    // B fragments: k-step 2j holds channels 32j+8c+{0,1 | 2,3}, k-step 2j+1 holds +{4,5 | 6,7}.
-    uint32_t bq[NSS][4];
-    {
-        const bf16* qrow = reinterpret_cast<const bf16*>(a.q) + ((long long)b * a.H_q + h * G + (n < G ? n : 0)) * D;
-#pragma unroll
-        for (int j = 0; j < NSS; ++j) {
-            float v[8];
-            const int e0 = 32 * j + 8 * c;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = e0 + i;
-                float qv = 0.f;
-                if (n < G) qv = __bfloat162float(qrow[e < D ? e : e - D]);
-                v[i] = e < D ? fminf(qv, 0.f) : fmaxf(qv, 0.f);
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
             }
-            bq[j][0] = pack_bf16(v[0], v[1]);
-            bq[j][1] = pack_bf16(v[2], v[3]);
-            bq[j][2] = pack_bf16(v[4], v[5]);
-            bq[j][3] = pack_bf16(v[6], v[7]);
+            if (bb < a.B) pref[bb] = run + incl - t;
+            run += __shfl_sync(0xffffffffu, incl, 31);
         }
+        if (lane == 0) pref[a.B] = run;
     }
+    __syncthreads();
+    const long long total = pref[a.B];
+    const long long nwarps = (long long)gridDim.x * kScoreWarps;
+    const long long gw = (long long)blockIdx.x * kScoreWarps + warp;
+    const long long g0 = total * gw / nwarps, g1 = total * (gw + 1) / nwarps;
+    const int ntile = (int)(g1 - g0);
 
-    float* sc_row = a.scores + ((long long)b * a.H_kv + h) * a.max_pages;
+    // tile index -> (sequence, KV head, first page); shared-memory lookups only
+    auto locate = [&](long long g, int& b, int& h, int& p0, int& P) {
+        int lo = 0, hi = a.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (pref[mid] <= g) lo = mid;
+            else hi = mid - 1;
+        }
+        b = lo;
+        P = pages[b];
+        const int tb = (P + 15) / 16;
+        const int local = (int)(g - pref[b]);
+        h = local / tb;
+        p0 = (local - h * tb) * 16;
+    };
+    int issued_row = -1;
+    auto issue = [&](int t) {
+        int b, h, p0, P;
+        locate(g0 + t, b, h, p0, P);
+        const int row = b * a.H_kv + h;
+        const bool newq = row != issued_row;
+        issued_row = row;
+        if (lane == 0) {
+            const int slot = t % kScoreStages;
+            const uint32_t bytes = (uint32_t)(min(16, P - p0) * C::PAGE_BYTES);
+            mbar_arrive_expect_tx(bars + slot, bytes);
+            bulk_load(ring + slot * SLOT, a.summ + ((((long long)b * a.H_kv + h) * a.max_pages) + p0) * 2LL * D,
+                      bytes, bars + slot);
+        }
+        // a new row's query heads are pulled into L2 now, read when the tile is consumed
+        if (newq && lane * 128 < G * D * 2)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(a.q) +
+                                                          ((long long)b * a.H_q + h * G) * D * 2 + lane * 128));
+    };
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < kScoreStages; ++i)
+        if (i < ntile) issue(i);
+
+    uint32_t bq[NSS][4];
+    int cur_row = -1;
     const int r = lane >> 2;
     const float ninf = __int_as_float(0xff800000);
     const bool h0 = 2 * c < G, h1 = 2 * c + 1 < G;
     for (int t = 0; t < ntile; ++t) {
+        int b, h, p0, P;
+        locate(g0 + t, b, h, p0, P);
+        const int row = b * a.H_kv + h;
         const int slot = t % kScoreStages;
         if (!mbar_wait_bounded(bars + slot, (uint32_t)((t / kScoreStages) & 1), a.status)) {
-            // Let the copies still in flight land (bounded) before giving up on this chunk.
+            // Let the copies still in flight land (bounded) before giving up.
             for (int k2 = t + 1; k2 < ntile && k2 < t + kScoreStages; ++k2)
                 mbar_wait_bounded(bars + (k2 % kScoreStages), (uint32_t)((k2 / kScoreStages) & 1), a.status);
             break;
         }
-        const unsigned vm = vmask[slot];
-        const uint8_t* tile = ring + slot * C::TILE;
-        const uint8_t* ta = tile + r * C::STRIDE + 16 * c;
-        const uint8_t* tb = ta + 8 * C::STRIDE;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint8_t* sl = ring + slot * SLOT;
+        if (row != cur_row) {
+            // B fragments of this row's query heads: k-step 2j holds channels
+            // 32j+8c+{0,1 | 2,3}, k-step 2j+1 holds +{4,5 | 6,7}
+            cur_row = row;
+            const bf16* qrow = reinterpret_cast<const bf16*>(a.q) + ((long long)b * a.H_q + h * G + (n < G ? n : 0)) * D;
 #pragma unroll
-        for (int j = 0; j < NSS; ++j) {
-            const uint4 ra = *reinterpret_cast<const uint4*>(ta + 64 * j);
-            const uint4 rb = *reinterpret_cast<const uint4*>(tb + 64 * j);
-            const uint32_t a0[4] = {ra.x, rb.x, ra.y, rb.y};
-            mma_bf16(acc, a0, bq[j][0], bq[j][1]);
-            const uint32_t a1[4] = {ra.z, rb.z, ra.w, rb.w};
-            mma_bf16(acc, a1, bq[j][2], bq[j][3]);
+            for (int jj = 0; jj < NSS; ++jj) {
+                float v[8];
+                const int e0 = 32 * jj + 8 * c;
+                const uint4 raw = *reinterpret_cast<const uint4*>(qrow + (e0 < D ? e0 : e0 - D));
+                const bf16* rv = reinterpret_cast<const bf16*>(&raw);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float qv = n < G ? __bfloat162float(rv[i]) : 0.f;
+                    v[i] = e0 < D ? fminf(qv, 0.f) : fmaxf(qv, 0.f);
+                }
+                bq[jj][0] = pack_bf16(v[0], v[1]);
+                bq[jj][1] = pack_bf16(v[2], v[3]);
+                bq[jj][2] = pack_bf16(v[4], v[5]);
+                bq[jj][3] = pack_bf16(v[6], v[7]);
+            }
         }
+        const uint8_t* ta = sl + r * C::PAGE_BYTES + 16 * c;
+        const uint8_t* tb = ta + 8 * C::PAGE_BYTES;
+        // four independent accumulator chains over the super-steps
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < NSS; ++jj) {
+            const uint4 ra = *reinterpret_cast<const uint4*>(ta + 64 * jj);
+            const uint4 rb = *reinterpret_cast<const uint4*>(tb + 64 * jj);
+            const uint32_t a0[4] = {ra.x, rb.x, ra.y, rb.y};
+            mma_bf16(acc[(2 * jj) & 3], a0, bq[jj][0], bq[jj][1]);
+            const uint32_t a1[4] = {ra.z, rb.z, ra.w, rb.w};
+            mma_bf16(acc[(2 * jj + 1) & 3], a1, bq[jj][2], bq[jj][3]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[0][e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
         // acc: pages r / r+8 x query heads 2c, 2c+1.  Max over the group's heads.
-        float s0 = fmaxf(h0 ? acc[0] : ninf, h1 ? acc[1] : ninf);
-        float s1 = fmaxf(h0 ? acc[2] : ninf, h1 ? acc[3] : ninf);
+        float s0 = fmaxf(h0 ? acc[0][0] : ninf, h1 ? acc[0][1] : ninf);
+        float s1 = fmaxf(h0 ? acc[0][2] : ninf, h1 ? acc[0][3] : ninf);
         s0 = fmaxf(s0, __shfl_xor_sync(0xffffffffu, s0, 1));
         s1 = fmaxf(s1, __shfl_xor_sync(0xffffffffu, s1, 1));
         s0 = fmaxf(s0, __shfl_xor_sync(0xffffffffu, s0, 2));
         s1 = fmaxf(s1, __shfl_xor_sync(0xffffffffu, s1, 2));
-        const int p0 = chunk_lo + (warp + kScoreWarps * t) * 16;
+        float* sc_row = a.scores + (long long)row * a.max_pages;
         if (c == 0) {
-            if (p0 + r < chunk_hi) sc_row[p0 + r] = (vm >> r) & 1u ? s0 : ninf;
-            if (p0 + r + 8 < chunk_hi) sc_row[p0 + r + 8] = (vm >> (r + 8)) & 1u ? s1 : ninf;
+            if (p0 + r < P) sc_row[p0 + r] = s0;
+            if (p0 + r + 8 < P) sc_row[p0 + r + 8] = s1;
         }
         __syncwarp();  // the slot has been read by every lane
-        if (t + kScoreStages < ntile) vmask[slot] = issue(t + kScoreStages);
+        if (t + kScoreStages < ntile) issue(t + kScoreStages);
     }
-
-    // Ticket: the last CTA of this row selects.
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const int prev = atomicAdd(a.counters + (long long)b * a.H_kv + h, 1);
-        s_last = (prev == nch - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    select_row(a, b, h, P, len, reinterpret_cast<uint32_t*>(ring_base));
-    if (threadIdx.x == 0) a.counters[(long long)b * a.H_kv + h] = 0;
-}
-
-int score_chunk_pages(int max_pages, int rows, int num_sms) {
-    // About two CTAs per SM resident; aim for ~3 waves, 128..1024 pages per CTA.
-    long long target = 6LL * num_sms;
-    long long per_row = (target + rows - 1) / (rows > 0 ? rows : 1);
-    int cp = (int)((max_pages + per_row - 1) / (per_row > 0 ? per_row : 1));
-    cp = ((cp + 63) / 64) * 64;
-    if (cp < 128) cp = 128;
-    if (cp > 1024) cp = 1024;
-    return cp;
 }
 
 template <int D>
-static cudaError_t launch_score_t(const ScoreSelectArgs& a, int chunk_pages, cudaStream_t st) {
+static cudaError_t launch_score_t(const ScoreSelectArgs& a, int grid, cudaStream_t st) {
     using C = ScoreCfg<D>;
-    const int nch = (a.max_pages + chunk_pages - 1) / chunk_pages;
-    dim3 grid(nch, a.H_kv, a.B), block(kScoreThreads);
     static_assert(C::BARS <= 128, "barriers must fit in front of the ring");
-    const size_t keys = (size_t)a.max_pages * sizeof(uint32_t);
-    const size_t smem = 128 /*alignment slack*/ + 128 /*barriers*/ + (((size_t)chunk_pages * 4 + 127) & ~(size_t)127) +
-                        (keys > (size_t)C::RING ? keys : (size_t)C::RING);
+    const size_t ring = (size_t)kScoreWarps * kScoreStages * C::TILE;
+    const size_t smem = 128 /*alignment slack*/ + 128 /*barriers*/ + ring + (2 * (size_t)a.B + 1) * sizeof(int);
     cudaError_t e = cudaFuncSetAttribute(score_select_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    score_select_kernel<D><<<grid, block, smem, st>>>(a, chunk_pages);
+    score_select_kernel<D><<<grid, kScoreThreads, smem, st>>>(a, 0);
     return cudaGetLastError();
 }
 
-cudaError_t launch_score_select(const ScoreSelectArgs& a, int chunk_pages, cudaStream_t st) {
+cudaError_t launch_score_select(const ScoreSelectArgs& a, int num_sms, cudaStream_t st) {
     if (a.B == 0) return cudaSuccess;
-    return a.D == 128 ? launch_score_t<128>(a, chunk_pages, st) : launch_score_t<64>(a, chunk_pages, st);
+    // persistent: two CTAs per SM, each warp streams an equal share of all tiles
+    const int grid = 2 * num_sms;
+    cudaError_t e = a.D == 128 ? launch_score_t<128>(a, grid, st) : launch_score_t<64>(a, grid, st);
+    if (e != cudaSuccess) return e;
+    // selection: one CTA per row, the row's keys in shared memory
+    const size_t smem = (size_t)a.max_pages * sizeof(uint32_t);
+    e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    select_kernel<<<(unsigned)((long long)a.B * a.H_kv), kSelThreads, smem, st>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace spd

@@ -271,7 +271,7 @@ SPD_API spd_status pages_summarize(const spd_dims* dims, const spd_bf16* K, cons
 }
 
 SPD_API spd_status pages_score_select(const spd_dims* dims, const spd_bf16* q, const spd_bf16* summ,
-                                      const int32_t* page_table, const int32_t* seq_lens,
+                                      const int32_t* seq_lens,
                                       const spd_budget_policy* policy, int32_t* sel, int32_t* nsel, int32_t k_max,
                                       float* scores, void* ws, size_t ws_bytes, void* stream) {
     spd_status st = check_dims(dims);
@@ -289,8 +289,9 @@ SPD_API spd_status pages_score_select(const spd_dims* dims, const spd_bf16* q, c
         return fail(SPD_ERR_INVALID_ARG, "k_max (%d) must be >= 1 and >= sink_pages + local_pages", k_max);
     if (dims->max_pages_per_seq > 32768)
         return fail(SPD_ERR_UNSUPPORTED, "max_pages_per_seq %d > 32768", dims->max_pages_per_seq);
+    if (dims->B > 16384) return fail(SPD_ERR_UNSUPPORTED, "pages_score_select supports B <= 16384");
     if (dims->B == 0) return SPD_OK;
-    if (!q || !summ || !page_table || !seq_lens || !sel || !nsel)
+    if (!q || !summ || !seq_lens || !sel || !nsel)
         return fail(SPD_ERR_INVALID_ARG, "NULL pointer argument");
     if (!aligned16(q) || !aligned16(summ)) return fail(SPD_ERR_INVALID_ARG, "q and summ must be 16-byte aligned");
     const size_t need = spd_score_select_workspace_size(dims);
@@ -302,7 +303,6 @@ SPD_API spd_status pages_score_select(const spd_dims* dims, const spd_bf16* q, c
     ScoreSelectArgs a;
     a.q = q;
     a.summ = summ;
-    a.page_table = page_table;
     a.seq_lens = seq_lens;
     a.pol = p;
     a.sel = sel;
@@ -318,8 +318,7 @@ SPD_API spd_status pages_score_select(const spd_dims* dims, const spd_bf16* q, c
     a.max_pages = dims->max_pages_per_seq;
     a.num_phys = dims->num_phys_pages;
     a.status = d->status;
-    const int cp = score_chunk_pages(a.max_pages, (int)rows, d->sms);
-    cudaError_t e = launch_score_select(a, cp, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_score_select(a, d->sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SPD_OK : cuda_fail(e, "pages_score_select launch");
 }
 

@@ -1,9 +1,11 @@
 // summarize.cu -- per-page key summaries: channel-wise min and max of the valid
-// keys of each (physical page, KV head).  These are the page metadata that the
-// Quest-style upper-bound score reads (Sparrow, "Control Study 2": the scoring
-// term of the cost model reads one summary per generated page).
+// keys of each (sequence, logical page, KV head).  These are the page metadata
+// that the Quest-style upper-bound score reads (Sparrow, "Control Study 2": the
+// scoring term of the cost model reads one summary per generated page).  They
+// are stored sequence-major, [B][H_kv][max_pages][2][D], so that scoring a
+// (sequence, KV head) row reads one contiguous stream.
 //
-// One warp per (page, KV head).  The tile is ps rows of D bf16 (contiguous);
+// One warp per (page, KV head).  The K tile is ps rows of D bf16 (contiguous);
 // lanes read 16-byte chunks so one warp instruction covers 512 contiguous
 // bytes, then lanes holding the same channels reduce with shuffles.  bf16
 // min/max is exact, so the result is bit-identical to any exact reference.
@@ -75,7 +77,8 @@ __global__ void __launch_bounds__(256) summarize_kernel(SummarizeArgs a) {
             }
         }
         if (r0 == 0) {
-            uint4* out = reinterpret_cast<uint4*>(a.summ + (phys * a.H_kv + h) * 2LL * D);
+            uint4* out = reinterpret_cast<uint4*>(
+                a.summ + (((long long)b * a.H_kv + h) * a.max_pages + p) * 2LL * D);
             out[ch] = *reinterpret_cast<uint4*>(mn);
             out[LPR + ch] = *reinterpret_cast<uint4*>(mx);
         }

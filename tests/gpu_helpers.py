@@ -28,7 +28,7 @@ class Gpu:
     def summarize(self, only_pages=None, summ=None):
         t, w = self.torch, self.w
         if summ is None:
-            summ = t.zeros((w.num_phys_pages, w.H_kv, 2, w.D), dtype=t.bfloat16, device="cuda")
+            summ = t.zeros((w.B, w.H_kv, w.max_pages_per_seq, 2, w.D), dtype=t.bfloat16, device="cuda")
         op = None if only_pages is None else t.as_tensor(np.asarray(only_pages, np.int32), device="cuda")
         self.spd.pages_summarize(self.dims, self.d["K"], self.d["page_table"], self.d["seq_lens"],
                                  summ, only_pages=op)
@@ -42,7 +42,7 @@ class Gpu:
         scores = t.full((w.B, w.H_kv, w.max_pages_per_seq), float("nan"), device="cuda")
         ws = self.ws(self.spd.spd_score_select_workspace_size(self.dims))
         self.spd.pages_score_select(self.dims, self.d["q"] if q is None else q, summ,
-                                    self.d["page_table"], self.d["seq_lens"],
+                                    self.d["seq_lens"],
                                     policy or w.policy, sel, nsel, k_max, ws, scores=scores)
         return sel, nsel, scores, ws
 

@@ -55,10 +55,10 @@ def test_validation_rejects_bad_shapes_without_touching_the_gpu(libspd):
     assert L.pages_summarize(None, None, None, None, None, 0, None, None) == 1
     pol = libspd.Policy(0, 8, 0, 0, 1, 0, 1, 1, 1, 4)
     # k_max below sink + local
-    assert L.pages_score_select(ctypes.byref(d), None, None, None, None, ctypes.byref(pol), None,
+    assert L.pages_score_select(ctypes.byref(d), None, None, None, ctypes.byref(pol), None,
                                 None, 3, None, None, 0, None) == 1
     pol_bad = libspd.Policy(1, 0, 0, 1, 0, 0, 1, 1, 1, 1)  # slope_den = 0
-    assert L.pages_score_select(ctypes.byref(d), None, None, None, None, ctypes.byref(pol_bad),
+    assert L.pages_score_select(ctypes.byref(d), None, None, None, ctypes.byref(pol_bad),
                                 None, None, 8, None, None, 0, None) == 1
     assert L.lse_merge(0, 4, 64, None, None, None, None, None) == 1
     assert L.lse_merge(2, 4, 80, None, None, None, None, None) == 2

@@ -30,7 +30,7 @@ def test_full_size_sampled(name, ps):
     for b in sample:
         for p in range(w.pages(b)):
             ph = w.page_table[b, p]
-            assert np.array_equal(got[ph], wl.f32_to_bf16_bits(s_ref[ph].astype(np.float32))), (b, p)
+            assert np.array_equal(got[b, :, p], wl.f32_to_bf16_bits(s_ref[ph].astype(np.float32))), (b, p)
     sc_ref = oracle.scores(w, s_ref, seqs=sample, threads=16)
     sel_ref, nsel_ref = oracle.select(w, sc_ref, seqs=sample, threads=16)
     for b in sample:

@@ -42,9 +42,8 @@ def test_summaries_bit_exact(case):
     got = summ_bits(summ)
     for b in range(w.B):
         for p in range(w.pages(b)):
-            ph = w.page_table[b, p]
-            exp = wl.f32_to_bf16_bits(ref["summ"][ph].astype(np.float32))
-            assert np.array_equal(got[ph], exp), (b, p)
+            exp = wl.f32_to_bf16_bits(ref["summ"][w.page_table[b, p]].astype(np.float32))
+            assert np.array_equal(got[b, :, p], exp), (b, p)
 
 
 def test_scores_and_selection(case):
@@ -196,17 +195,17 @@ def test_incremental_summary_matches_full():
     g = Gpu(w)
     full = summ_bits(g.summarize())
     last = [b * w.max_pages_per_seq + (int(w.seq_lens[b]) - 1) // 16 for b in range(w.B)]
-    sentinel = g.torch.full((w.num_phys_pages, w.H_kv, 2, w.D), 3.0, dtype=g.torch.bfloat16,
+    sentinel = g.torch.full((w.B, w.H_kv, w.max_pages_per_seq, 2, w.D), 3.0, dtype=g.torch.bfloat16,
                             device="cuda")
     inc = summ_bits(g.summarize(only_pages=last, summ=sentinel))
     assert g.sync_status() == 0
-    touched = {int(w.page_table[s // w.max_pages_per_seq, s % w.max_pages_per_seq]) for s in last}
     s3 = wl.f32_to_bf16_bits(np.float32(3.0))
-    for ph in range(w.num_phys_pages):
-        if ph in touched:
-            assert np.array_equal(inc[ph], full[ph])
-        else:
-            assert np.all(inc[ph] == s3)
+    for b in range(w.B):
+        for p in range(w.max_pages_per_seq):
+            if b * w.max_pages_per_seq + p in last:
+                assert np.array_equal(inc[b, :, p], full[b, :, p])
+            else:
+                assert np.all(inc[b, :, p] == s3)
 
 
 def test_workspace_reuse_gives_identical_results():

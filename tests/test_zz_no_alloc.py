@@ -32,11 +32,11 @@ def test_noalloc_matches_workspace_entry_point_twice(splits):
     w = wl.named("q8b", B=6, len_lo=600, len_hi=2500, threads=4)
     d = wl.to_device(w)
     dims = spd.dims_of(w.B, w.H_q, w.H_kv, w.D, w.page_size, w.max_pages_per_seq, w.num_phys_pages)
-    summ = torch.empty((w.num_phys_pages, w.H_kv, 2, w.D), dtype=torch.bfloat16, device="cuda")
+    summ = torch.empty((w.B, w.H_kv, w.max_pages_per_seq, 2, w.D), dtype=torch.bfloat16, device="cuda")
     spd.pages_summarize(dims, d["K"], d["page_table"], d["seq_lens"], summ)
     sel = torch.empty((w.B, w.H_kv, w.k_max), dtype=torch.int32, device="cuda")
     nsel = torch.empty((w.B, w.H_kv), dtype=torch.int32, device="cuda")
-    spd.pages_score_select(dims, d["q"], summ, d["page_table"], d["seq_lens"], w.policy, sel, nsel,
+    spd.pages_score_select(dims, d["q"], summ, d["seq_lens"], w.policy, sel, nsel,
                            w.k_max, spd.workspace(spd.spd_score_select_workspace_size(dims)))
 
     def run(fn, **kw):
