@@ -47,15 +47,18 @@ struct UnitInfo {
     int nsplit;  // units of this row
 };
 
-template <int D, int PS, int NMT>
+template <int D, int PS, int NMT, bool SPARSE>
 struct AttnCfg {
     static constexpr int TILE = PS * D * 2;  // bytes of one K (or V) tile
     static constexpr int SLOT = 2 * TILE;
-    // ring depth: ~24-64 KB of K/V in flight per worker
-    static constexpr int STAGES = NMT == 1 ? (SLOT <= 8192 ? 3 : 2) : (SLOT <= 8192 ? 4 : (SLOT <= 16384 ? 3 : 2));
+    // ring depth: ~32-64 KB of K/V in flight per worker
+    static constexpr int STAGES = SLOT <= 8192 ? 4 : (SLOT <= 16384 ? 3 : 2);
     static constexpr int THREADS = (NMT + 1) * 32;  // consumers + one producer warp
     static constexpr int RP = NMT * 16;             // padded rows
-    static constexpr int QBYTES = RP * D * 2;
+    // A Q buffer holds the unit's R real rows (decode: R = G <= 8; verify:
+    // R <= RP); padding rows are zero in registers.
+    static constexpr int QROWS = SPARSE ? 8 : RP;
+    static constexpr int QBYTES = QROWS * D * 2;
     static constexpr int NQ = STAGES + 1;           // Q buffers: at most STAGES + 1 units are live
     static constexpr int FIFO = 8;                  // unit-info entries (>= STAGES + 1)
     static constexpr int OFF_Q = STAGES * SLOT;
@@ -71,10 +74,10 @@ constexpr int kEndOfWork = -2;  // slot_meta.x: no more items
 constexpr float kRescale = 8.f;  // log2 headroom before the running max moves
 
 template <int D, int PS, int NMT, bool SPARSE>
-__global__ void __launch_bounds__(AttnCfg<D, PS, NMT>::THREADS)
+__global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV) {
-    using C = AttnCfg<D, PS, NMT>;
+    using C = AttnCfg<D, PS, NMT, SPARSE>;
     constexpr int STAGES = C::STAGES;
     constexpr int KSTEPS = D / 16;
     constexpr int NT_O = D / 8;
@@ -96,9 +99,6 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT>::THREADS)
     const int R = a.T * G;
     const float NEG_INF = __int_as_float(0xff800000);
 
-    // Padding rows of the Q buffers stay zero; only the R real rows are copied.
-    for (int i = tid; i < C::NQ * C::QBYTES / 16; i += C::THREADS)
-        reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(full + i, 1);
@@ -106,8 +106,6 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT>::THREADS)
         }
         mbar_fence_init();
     }
-    // generic-proxy zeros of the Q buffers before any bulk copy into them
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
 
     // Output row r of a (b, h) row -> index into o ([B][T][H_q]) and lse.
@@ -283,10 +281,10 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT>::THREADS)
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
                 const int d0 = kk * 16 + 2 * c4;
-                qa[kk][0] = *reinterpret_cast<const uint32_t*>(qsm + (qr0 * D + d0) * 2);
-                qa[kk][1] = *reinterpret_cast<const uint32_t*>(qsm + (qr1 * D + d0) * 2);
-                qa[kk][2] = *reinterpret_cast<const uint32_t*>(qsm + (qr0 * D + d0 + 8) * 2);
-                qa[kk][3] = *reinterpret_cast<const uint32_t*>(qsm + (qr1 * D + d0 + 8) * 2);
+                qa[kk][0] = qr0 < R ? *reinterpret_cast<const uint32_t*>(qsm + (qr0 * D + d0) * 2) : 0u;
+                qa[kk][1] = qr1 < R ? *reinterpret_cast<const uint32_t*>(qsm + (qr1 * D + d0) * 2) : 0u;
+                qa[kk][2] = qr0 < R ? *reinterpret_cast<const uint32_t*>(qsm + (qr0 * D + d0 + 8) * 2) : 0u;
+                qa[kk][3] = qr1 < R ? *reinterpret_cast<const uint32_t*>(qsm + (qr1 * D + d0 + 8) * 2) : 0u;
             }
             m0 = m1 = NEG_INF;
             l0 = l1 = 0.f;
@@ -524,7 +522,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT>::THREADS)
 
 template <int D, int PS, int NMT, bool SPARSE>
 int attn_ctas_per_sm_t() {
-    using C = AttnCfg<D, PS, NMT>;
+    using C = AttnCfg<D, PS, NMT, SPARSE>;
     int n = 0;
     // The answer depends on the kernel's dynamic shared-memory limit: set it first
     // so the launch shape is the same before and after the kernel's first launch.
@@ -539,7 +537,7 @@ int attn_ctas_per_sm_t() {
 template <int D, int PS, int NMT, bool SPARSE>
 cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           cudaStream_t st) {
-    using C = AttnCfg<D, PS, NMT>;
+    using C = AttnCfg<D, PS, NMT, SPARSE>;
     auto kern = attn_kernel<D, PS, NMT, SPARSE>;
     const int per_sm = attn_ctas_per_sm_t<D, PS, NMT, SPARSE>();
     const long long units = (long long)a.B * a.H_kv * a.num_splits;

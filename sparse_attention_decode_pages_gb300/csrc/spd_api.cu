@@ -128,16 +128,22 @@ spd_status check_dims(const spd_dims* d) {
 
 int pages_per_split_floor(int ps) { return ps >= 64 ? 2 : (ps == 32 ? 4 : 8); }
 
-// Splits per row: several units per persistent worker (units_per_worker), with
-// at least a few pages per unit, so the atomic unit queue balances the workers
-// and the last unit to finish is short.
-int splits_for(long long rows, int items, long long workers, int floor_items, int units_per_worker, int req) {
+// Splits per row.  Sparse rows are short and about equal (k_max pages), so a
+// row is one unit unless there are too few rows to occupy the persistent
+// workers (a whole-row unit needs no partials or merge).  Dense rows differ in
+// length by up to 2x, so they are cut into about units_per_worker units per
+// worker for the queue to balance.  Each unit keeps at least floor_items pages.
+int splits_for(long long rows, int items, long long workers, int floor_items, int units_per_worker,
+               int req) {
     int S = req;
     if (S <= 0) {
-        const long long target = units_per_worker * workers;
-        S = (int)((target + rows - 1) / (rows > 0 ? rows : 1));
-        const int max_s = (items + floor_items - 1) / floor_items;
-        if (S > max_s) S = max_s;
+        S = 1;
+        const long long want = units_per_worker * workers;
+        if (rows > 0 && (units_per_worker > 1 ? rows < want : 2 * rows < want)) {
+            S = (int)((want + rows - 1) / rows);
+            const int max_s = (items + floor_items - 1) / floor_items;
+            if (S > max_s) S = max_s;
+        }
     }
     if (S > items) S = items;
     if (S < 1) S = 1;
@@ -148,14 +154,14 @@ int splits_for(long long rows, int items, long long workers, int floor_items, in
 int sparse_splits(const spd_dims* d, int k_max, int req, int sms) {
     const long long rows = (long long)d->B * d->H_kv;
     const long long workers = (long long)sms * occ_sparse_attn(d->D, d->page_size);
-    return splits_for(rows, k_max, workers, pages_per_split_floor(d->page_size), 4, req);
+    return splits_for(rows, k_max, workers, pages_per_split_floor(d->page_size), 1, req);
 }
 
 int dense_splits(const spd_dims* d, int T, int req, int sms) {
     const long long rows = (long long)d->B * d->H_kv;
     const int mt = attn_mtiles(T, d->H_q / d->H_kv);
     const long long workers = (long long)sms * occ_dense_attn(d->D, d->page_size, mt);
-    return splits_for(rows, d->max_pages_per_seq, workers, 2 * pages_per_split_floor(d->page_size), 12, req);
+    return splits_for(rows, d->max_pages_per_seq, workers, 2 * pages_per_split_floor(d->page_size), 4, req);
 }
 
 struct AttnWs {
