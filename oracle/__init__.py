@@ -56,8 +56,13 @@ def lib():
         L.oracle_sparse_attn_seq.argtypes = [i, i, i, i, i, P, P, P, P, P, i, P, P, i, d, P, P]
         L.oracle_merge_row.argtypes = [i, i, P, P, P, P]
         L.oracle_verify_seq.argtypes = [i, i, i, i, i, i, P, P, P, P, P, i, d, P, P]
+        L.oracle_append_seq.argtypes = [i, i, i, i, i, P, P, P, P, i, P, P]
+        L.oracle_spec_accept_seq.argtypes = [i, i, P, P, P, P, ctypes.c_float, P]
+        L.oracle_spec_accept_seq.restype = i
+        L.oracle_select_top_p_seq.argtypes = [i, i, i, P, i, d, d, i, i, i, P, P]
         for f in ("oracle_summarize_seq", "oracle_score_seq", "oracle_select_seq",
-                  "oracle_sparse_attn_seq", "oracle_merge_row", "oracle_verify_seq"):
+                  "oracle_sparse_attn_seq", "oracle_merge_row", "oracle_verify_seq",
+                  "oracle_append_seq", "oracle_select_top_p_seq"):
             getattr(L, f).restype = None
         _lib = L
     return _lib
@@ -200,3 +205,59 @@ def decode_step(w, threads=None):
     sel, nsel = select(w, sc, threads=threads)
     o, lse = sparse_attn(w, sel, nsel, threads=threads)
     return dict(summ=summ, scores=sc, sel=sel, nsel=nsel, o=o, lse=lse)
+
+
+def append(w, T, k_new, v_new, seqs=None, threads=None):
+    """Row f1: (K, V) copies of the cache with the T newest tokens of each sequence
+    written from k_new / v_new (bf16 bits [B][T][H_kv][D]); the inputs are untouched."""
+    L = lib()
+    K, V = w.K.copy(), w.V.copy()
+    k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+    assert k_new.shape == (w.B, T, w.H_kv, w.D) and v_new.shape == k_new.shape
+    _run(lambda b: L.oracle_append_seq(T, w.H_kv, w.D, w.page_size, w.max_pages_per_seq, _p(K),
+                                       _p(V), _p(w.page_table), _p(w.seq_lens), b, _p(k_new),
+                                       _p(v_new)),
+         _seqs(w, seqs), threads)
+    return K, V
+
+
+def spec_accept(p, q, draft, u_acc, u_res):
+    """Row f2: exact speculative sampling per sequence.
+
+    p float32 [B][k][n], q float32 [B][k+1][n], draft int32 [B][k], u_acc float32
+    [B][k], u_res float32 [B] -> (n_accepted int32 [B], tokens int32 [B][k+1])."""
+    L = lib()
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    draft = np.ascontiguousarray(draft, dtype=np.int32)
+    u_acc = np.ascontiguousarray(u_acc, dtype=np.float32)
+    u_res = np.ascontiguousarray(u_res, dtype=np.float32)
+    B, k, n = p.shape
+    assert q.shape == (B, k + 1, n) and draft.shape == (B, k) and u_acc.shape == (B, k)
+    tokens = np.full((B, k + 1), -1, dtype=np.int32)
+    nacc = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        nacc[b] = L.oracle_spec_accept_seq(k, n, p[b].ctypes.data, q[b].ctypes.data,
+                                           draft[b].ctypes.data, u_acc[b].ctypes.data,
+                                           float(u_res[b]), tokens[b].ctypes.data)
+    return nacc, tokens
+
+
+def select_top_p(w, sc, top_p, score_scale=None, k_max=None, policy=None, seqs=None, threads=None):
+    """Row f3: top-p page selection -> (sel int32 [B][H_kv][k_max], nsel int32 [B][H_kv])."""
+    L = lib()
+    pol = w.policy if policy is None else policy
+    k_max = w.k_max if k_max is None else k_max
+    score_scale = w.scale if score_scale is None else score_scale
+    sel = np.full((w.B, w.H_kv, k_max), -1, dtype=np.int32)
+    nsel = np.zeros((w.B, w.H_kv), dtype=np.int32)
+    sc = np.ascontiguousarray(sc, dtype=np.float64)
+
+    def one(b):
+        L.oracle_select_top_p_seq(w.H_kv, w.page_size, w.max_pages_per_seq, sc[b].ctypes.data,
+                                  int(w.seq_lens[b]), float(top_p), float(score_scale),
+                                  pol.sink_pages, pol.local_pages, k_max, sel[b].ctypes.data,
+                                  nsel[b].ctypes.data)
+    _run(one, _seqs(w, seqs), threads)
+    return sel, nsel

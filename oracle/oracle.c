@@ -341,3 +341,152 @@ void oracle_verify_seq(int T, int H_q, int H_kv, int D, int ps, int max_pages, c
     free(ts);
     free(z);
 }
+
+/*
+ * Row f1 -- appending tokens to the paged cache.  The T newest tokens of
+ * sequence b take the positions len_b - T .. len_b - 1 (len_b already counts
+ * them): position pos lives in logical page pos / ps, slot pos % ps, of the
+ * physical page page_table[b][pos / ps].  k_new and v_new are [B][T][H_kv][D]
+ * bf16 bit patterns, copied bit for bit into K and V.  The summaries of the
+ * pages this touches are then, by definition, oracle_summarize_seq over the
+ * updated cache.  Positions below 0 (len_b < T) are not written.
+ */
+void oracle_append_seq(int T, int H_kv, int D, int ps, int max_pages, uint16_t *K, uint16_t *V,
+                       const int32_t *page_table, const int32_t *seq_lens, int b,
+                       const uint16_t *k_new, const uint16_t *v_new)
+{
+    int len = seq_lens[b];
+    for (int t = 0; t < T; ++t) {
+        int pos = len - T + t;
+        if (pos < 0) continue;
+        long phys = page_table[(size_t)b * max_pages + pos / ps];
+        for (int h = 0; h < H_kv; ++h) {
+            size_t src = (((size_t)b * T + t) * H_kv + h) * D;
+            size_t dst = (((size_t)phys * H_kv + h) * ps + pos % ps) * D;
+            for (int d = 0; d < D; ++d) {
+                K[dst + d] = k_new[src + d];
+                V[dst + d] = v_new[src + d];
+            }
+        }
+    }
+}
+
+/*
+ * A draw from the unnormalised weights w[0..n) with a uniform u in [0, 1):
+ * the smallest x whose running sum exceeds u * sum(w).  If rounding leaves
+ * no such x, the last x with w[x] > 0.  All weights zero: -1.
+ */
+static int draw(const double *w, int n, double u)
+{
+    double total = 0.0;
+    for (int x = 0; x < n; ++x) total += w[x];
+    if (!(total > 0.0)) return -1;
+    double target = u * total, run = 0.0;
+    int last = -1;
+    for (int x = 0; x < n; ++x) {
+        if (w[x] > 0.0) last = x;
+        run += w[x];
+        if (run > target) return x;
+    }
+    return last;
+}
+
+/*
+ * Row f2 -- exact speculative sampling (the S3R abstract: responses come from
+ * full-attention verification followed by exact speculative sampling, so they
+ * follow the dense policy).  The rule is the standard one for a drafter
+ * distribution p and a target distribution q over a vocabulary of n tokens:
+ *   for i = 0 .. k-1, with x = draft[i]: accept iff u_acc[i] * p_i(x) < q_i(x)
+ *   (accept with probability min(1, q_i(x) / p_i(x)));
+ *   at the first rejection j, emit a draw (u_res) from max(0, q_j - p_j), or
+ *   from q_j when that residual is zero everywhere;
+ *   if all k drafts are accepted, emit a bonus draw (u_res) from q_k.
+ * p is [k][n] and q is [k+1][n] (fp32 probabilities, widened exactly; the
+ * products u * p of two fp32 values are exact in double).  tokens[0..k]
+ * receives the accepted drafts then the emitted token, -1 after it; the
+ * return value is the number of accepted drafts.
+ */
+int oracle_spec_accept_seq(int k, int n, const float *p, const float *q, const int32_t *draft,
+                           const float *u_acc, float u_res, int32_t *tokens)
+{
+    int acc = 0;
+    while (acc < k) {
+        int x = draft[acc];
+        double px = p[(size_t)acc * n + x], qx = q[(size_t)acc * n + x];
+        if (!((double)u_acc[acc] * px < qx)) break;
+        tokens[acc] = x;
+        ++acc;
+    }
+    double *w = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    const float *qr = q + (size_t)acc * n;
+    int tok;
+    if (acc < k) {
+        const float *pr = p + (size_t)acc * n;
+        for (int x = 0; x < n; ++x) {
+            double r = (double)qr[x] - (double)pr[x];
+            w[x] = r > 0.0 ? r : 0.0;
+        }
+        tok = draw(w, n, (double)u_res);
+        if (tok < 0) {
+            for (int x = 0; x < n; ++x) w[x] = qr[x] > 0.f ? (double)qr[x] : 0.0;
+            tok = draw(w, n, (double)u_res);
+        }
+    } else {
+        for (int x = 0; x < n; ++x) w[x] = qr[x] > 0.f ? (double)qr[x] : 0.0;
+        tok = draw(w, n, (double)u_res);
+    }
+    free(w);
+    tokens[acc] = tok;
+    for (int i = acc + 1; i <= k; ++i) tokens[i] = -1;
+    return acc;
+}
+
+/*
+ * Row f3 -- query-dependent (top-p) page selection for every KV head of
+ * sequence b: instead of a fixed number of pages, the smallest set whose
+ * share of the page weight reaches top_p.  A page's weight is
+ * w(p) = exp(score_scale * (score(p) - max_p' score(p'))) over the P_b
+ * pages (the score is an upper bound of q.k, so w is a softmax over pages of
+ * the bound logits).  The mandatory pages are taken first; then the
+ * remaining pages in score order (descending; equal scores: lower id first)
+ * while the selected weight is below top_p * sum_p w(p) and fewer than k_max
+ * pages are held.  The list is written in ascending page order.
+ */
+void oracle_select_top_p_seq(int H_kv, int ps, int max_pages, const double *scores, int len,
+                             double top_p, double score_scale, int sink, int local, int k_max,
+                             int32_t *sel, int32_t *nsel)
+{
+    int P = pages_of(len, ps);
+    ranked *cand = (ranked *)malloc(sizeof(ranked) * (P > 0 ? P : 1));
+    int *pick = (int *)malloc(sizeof(int) * (P > 0 ? P : 1));
+    for (int h = 0; h < H_kv; ++h) {
+        const double *s = scores + (size_t)h * max_pages;
+        double smax = -INFINITY;
+        for (int p = 0; p < P; ++p)
+            if (s[p] > smax) smax = s[p];
+        double total = 0.0;
+        for (int p = 0; p < P; ++p) total += exp(score_scale * (s[p] - smax));
+        double need = top_p * total, held = 0.0;
+        int n = 0, nc = 0;
+        for (int p = 0; p < P; ++p) {
+            if (is_mandatory(p, P, sink, local)) {
+                pick[n++] = p;
+                held += exp(score_scale * (s[p] - smax));
+            } else {
+                cand[nc].s = s[p];
+                cand[nc].p = p;
+                ++nc;
+            }
+        }
+        qsort(cand, nc, sizeof(ranked), by_score_then_id);
+        for (int i = 0; i < nc && held < need && n < k_max; ++i) {
+            pick[n++] = cand[i].p;
+            held += exp(score_scale * (cand[i].s - smax));
+        }
+        qsort(pick, n, sizeof(int), ascending);
+        for (int i = 0; i < n; ++i) sel[(size_t)h * k_max + i] = pick[i];
+        nsel[h] = n;
+    }
+    free(cand);
+    free(pick);
+}
