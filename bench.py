@@ -4,19 +4,21 @@
 One step is one pass of the hot path over one batch (B = 64 sequences, 32 query
 / 8 KV heads, head dim 128, contexts 8K..16K, page size 16, budget 64 pages):
 
-  a1  summary refresh of the page each sequence's newest token landed in
-      (pages_summarize on B listed pages),
+  f1  the step's new token appended to each sequence's cache, with the
+      summary of its page rewritten (kv_append_refresh, T = 1; the a1
+      summaries of the rest of the cache are resident),
   a2-a4  pages_score_select (upper-bound scores of every page, top-k budget),
   a5-a6  sparse_decode_attn (split-K over the selected pages, fused merge),
   a7  dense_verify_attn of k+1 = 7 drafted positions over the full cache.
 
 The headline metric is sparse decode-attention tokens/s (B tokens per pass of
-a1-a6); a7 is timed in the same steps and reported under "dense_verify".  Each
+f1 and a2-a6); a7 is timed in the same steps and reported under "dense_verify".  Each
 kernel is timed with CUDA events on the launching stream; L2 is evicted between timed passes
 (a 512 MiB read, outside the events; a write flush would leave ~L2-size of
 dirty lines to be written back during the next timed kernel).  The KV cache and the
 page summaries are resident in HBM (they are the cache); e2e adds, per step,
-the host->device copy of the step's inputs (q, seq_lens, page_table) from
+the host->device copy of the step's inputs (q, the new token's K / V,
+seq_lens, page_table) from
 pinned memory and the device->host copy of o and lse.
 
 --impl reference times the fp64 CPU oracle (there is no other reference
@@ -80,7 +82,13 @@ def algorithmic_bytes(w, nsel):
             toks = sum(min(ps, L - p * ps) for p in pages)
             kv += toks * 4 * D
     qo = w.B * w.H_q * D * 2 * 2 + w.B * w.H_q * 4
-    refresh = w.B * H_kv * (ps * D * 2 + 4 * D)  # a1: last page read, its summary written
+    # f1: the new token's K and V written, the older tokens of its page read, the
+    # page summary written
+    refresh = 0
+    for b in range(w.B):
+        L = int(w.seq_lens[b])
+        old = (L - 1) - ((L - 1) // ps) * ps
+        refresh += H_kv * (2 * D * 2 + old * D * 2 + 4 * D) + H_kv * 2 * D * 2  # + k_new/v_new read
     return dict(attn=kv + qo, score=summ + w.B * w.H_q * D * 2, refresh=refresh,
                 step=kv + summ + qo + refresh)
 
@@ -173,8 +181,15 @@ def run_gpu(args):
     dims = spd.dims_of(w.B, w.H_q, w.H_kv, w.D, w.page_size, w.max_pages_per_seq, w.num_phys_pages)
     summ = torch.empty((w.B, w.H_kv, w.max_pages_per_seq, 2, w.D), dtype=torch.bfloat16, device=dev)
     spd.pages_summarize(dims, d["K"], d["page_table"], d["seq_lens"], summ)  # prefill
-    last = torch.tensor([b * w.max_pages_per_seq + (int(w.seq_lens[b]) - 1) // w.page_size
-                         for b in range(w.B)], dtype=torch.int32, device=dev)
+    # the step's new token: its K / V are the ones already at position len - 1, so
+    # every pass writes the same values and the cache stays the same workload
+    k_new = torch.empty((w.B, 1, w.H_kv, w.D), dtype=torch.bfloat16, device=dev)
+    v_new = torch.empty_like(k_new)
+    for b in range(w.B):
+        L = int(w.seq_lens[b])
+        ph = int(w.page_table[b, (L - 1) // w.page_size])
+        k_new[b, 0] = d["K"][ph, :, (L - 1) % w.page_size]
+        v_new[b, 0] = d["V"][ph, :, (L - 1) % w.page_size]
     k_max = w.k_max
     sel = torch.empty((w.B, w.H_kv, k_max), dtype=torch.int32, device=dev)
     nsel = torch.empty((w.B, w.H_kv), dtype=torch.int32, device=dev)
@@ -202,7 +217,8 @@ def run_gpu(args):
     def sparse_pass(ev=None):
         if ev:
             ev[0].record(stream)
-        spd.pages_summarize(dims, d["K"], d["page_table"], d["seq_lens"], summ, only_pages=last)
+        spd.kv_append_refresh(dims, 1, d["K"], d["V"], d["page_table"], d["seq_lens"], k_new, v_new,
+                              summ)
         if ev:
             ev[1].record(stream)
         spd.pages_score_select(dims, d["q"], summ, d["seq_lens"], policy, sel,
@@ -274,6 +290,8 @@ def run_gpu(args):
     q_h = d["q"].cpu().pin_memory()
     sl_h = d["seq_lens"].cpu().pin_memory()
     pt_h = d["page_table"].cpu().pin_memory()
+    kn_h = k_new.cpu().pin_memory()
+    vn_h = v_new.cpu().pin_memory()
     o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     e2e_ms = []
@@ -284,6 +302,8 @@ def run_gpu(args):
         d["q"].copy_(q_h, non_blocking=True)
         d["seq_lens"].copy_(sl_h, non_blocking=True)
         d["page_table"].copy_(pt_h, non_blocking=True)
+        k_new.copy_(kn_h, non_blocking=True)
+        v_new.copy_(vn_h, non_blocking=True)
         sparse_pass()
         o_h.copy_(o, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
@@ -291,7 +311,7 @@ def run_gpu(args):
         eb.synchronize()
         if i >= args.warmup:
             e2e_ms.append(ea.elapsed_time(eb))
-    h2d = q_h.numel() * 2 + sl_h.numel() * 4 + pt_h.numel() * 4
+    h2d = q_h.numel() * 2 + sl_h.numel() * 4 + pt_h.numel() * 4 + (kn_h.numel() + vn_h.numel()) * 2
     d2h = o_h.numel() * 2 + lse_h.numel() * 4
 
     # max over ranks
@@ -341,7 +361,7 @@ def run_gpu(args):
                 "l2": "evicted between timed passes by reading a 512 MiB buffer (outside the events)",
                 "splits": args.splits, "verify_splits": args.vsplits,
             },
-            "step_ms": {"a1_refresh": float(np.mean(t_ref)), "a2_a4_score_select": float(np.mean(t_sel)),
+            "step_ms": {"f1_append_refresh": float(np.mean(t_ref)), "a2_a4_score_select": float(np.mean(t_sel)),
                         "a5_a6_sparse_attn": ms_att},
             "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s",
                               "frac": step_gbs / peak, "bytes": nbytes["step"],
@@ -357,7 +377,7 @@ def run_gpu(args):
                              / (ms_ver * 1e-3) / 1e12},
             "e2e": {"value": world * w.B / (ms_e2e * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms": ms_e2e},
-            # per step: summarize (a1), score + select (2), sparse attention with its
+            # per step: append + refresh (f1), score + select (2), sparse attention with its
             # fused merge (1), dense verification (1)
             "gpu_launches": args.steps * 5,
             "clocks": clocks,

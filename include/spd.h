@@ -72,6 +72,7 @@ typedef enum {
 #define SPD_DEV_BAD_PAGE 0x1u  /* a page-table entry outside [0, num_phys_pages) */
 #define SPD_DEV_BAD_SEL 0x2u   /* a selected page id outside the sequence, or nsel > k_max */
 #define SPD_DEV_TIMEOUT 0x4u   /* a bounded wait on an asynchronous copy ran out */
+#define SPD_DEV_BAD_LEN 0x8u   /* kv_append_refresh: seq_lens[b] < T or beyond the page table */
 
 /*
  * Problem shape.  Supported: D in {64, 128}; page_size in {16, 32, 64};
@@ -147,6 +148,33 @@ size_t spd_dense_verify_workspace_size(const spd_dims *dims, int32_t T, int32_t 
 spd_status pages_summarize(const spd_dims *dims, const spd_bf16 *K, const int32_t *page_table,
                            const int32_t *seq_lens, const int32_t *only_pages, int32_t n_only,
                            spd_bf16 *summ, void *stream);
+
+/*
+ * kv_append_refresh -- appends the T newest tokens of every sequence to the
+ * paged cache and rewrites the summaries of the pages they land in, in one
+ * kernel (the per-step cache update before scoring: one token per decode
+ * step; after verification, the T drafted positions rewritten with the
+ * target's keys and values).  KV pages: S3R Figure 1(c); the per-step scoring
+ * read of the summaries: Sparrow, "Control Study 2".
+ *
+ * seq_lens[b] already counts the new tokens: token t (0 <= t < T) goes to
+ * position pos = seq_lens[b] - T + t, i.e. slot pos % page_size of physical
+ * page page_table[b][pos / page_size], for every KV head:
+ *   K[phys][h][slot][:] = k_new[b][t][h][:],  V[...] = v_new[b][t][h][:]
+ * (k_new, v_new bf16 [B][T][H_kv][D], copied bit for bit).  Every page that
+ * receives a token gets summ[b][h][p] = min / max over all its valid tokens
+ * after the write -- the same bits pages_summarize would write -- whatever
+ * the summary held before.  Other pages and cache slots are untouched.
+ * Supported: 1 <= T <= 4096.  A sequence with seq_lens[b] < T or
+ * seq_lens[b] > max_pages_per_seq * page_size is skipped and sets
+ * SPD_DEV_BAD_LEN; a page id outside [0, num_phys_pages) sets SPD_DEV_BAD_PAGE.
+ * K, V, k_new, v_new and summ must be 16-byte aligned.  Sequences must not
+ * share the physical pages they append to.
+ */
+spd_status kv_append_refresh(const spd_dims *dims, int32_t T, spd_bf16 *K, spd_bf16 *V,
+                             const int32_t *page_table, const int32_t *seq_lens,
+                             const spd_bf16 *k_new, const spd_bf16 *v_new, spd_bf16 *summ,
+                             void *stream);
 
 /*
  * pages_score_select -- query-aware page scoring plus budgeted top-k

@@ -83,9 +83,10 @@ def lib():
         L.sparse_decode_attn_noalloc.argtypes = [DP, P, P, P, P, P, P, P, i32, i32, ctypes.c_float,
                                                  P, P, P]
         L.lse_merge.argtypes = [i32, i32, i32, P, P, P, P, P]
+        L.kv_append_refresh.argtypes = [DP, i32, P, P, P, P, P, P, P, P]
         for f in ("spd_device_status", "pages_summarize", "pages_score_select",
                   "sparse_decode_attn", "dense_verify_attn", "lse_merge",
-                  "sparse_decode_attn_noalloc"):
+                  "sparse_decode_attn_noalloc", "kv_append_refresh"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -159,6 +160,13 @@ def pages_summarize(dims: Dims, K, page_table, seq_lens, summ, only_pages=None, 
     n_only = 0 if only_pages is None else only_pages.numel()
     _check(lib().pages_summarize(ctypes.byref(dims), _ptr(K), _ptr(page_table), _ptr(seq_lens),
                                  _ptr(only_pages), n_only, _ptr(summ), _stream(stream)))
+
+
+def kv_append_refresh(dims: Dims, T: int, K, V, page_table, seq_lens, k_new, v_new, summ,
+                      stream=None):
+    _check(lib().kv_append_refresh(ctypes.byref(dims), T, _ptr(K), _ptr(V), _ptr(page_table),
+                                   _ptr(seq_lens), _ptr(k_new), _ptr(v_new), _ptr(summ),
+                                   _stream(stream)))
 
 
 def pages_score_select(dims: Dims, q, summ, seq_lens, policy, sel, nsel, k_max: int, ws,

@@ -23,6 +23,20 @@ struct SummarizeArgs {
 };
 cudaError_t launch_summarize(const SummarizeArgs& a, cudaStream_t st);
 
+struct AppendArgs {
+    uint16_t* K;
+    uint16_t* V;
+    const int32_t* page_table;
+    const int32_t* seq_lens;
+    const uint16_t* k_new;  // [B][T][H_kv][D]
+    const uint16_t* v_new;
+    uint16_t* summ;         // [B][H_kv][max_pages][2][D]
+    int B, T, H_kv, D, ps, max_pages;
+    long long num_phys;
+    unsigned* status;
+};
+cudaError_t launch_append_refresh(const AppendArgs& a, cudaStream_t st);
+
 struct ScoreSelectArgs {
     const uint16_t* q;
     const uint16_t* summ;  // [B][H_kv][max_pages][2][D]

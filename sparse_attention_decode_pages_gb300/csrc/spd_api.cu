@@ -276,6 +276,40 @@ SPD_API spd_status pages_summarize(const spd_dims* dims, const spd_bf16* K, cons
     return e == cudaSuccess ? SPD_OK : cuda_fail(e, "pages_summarize launch");
 }
 
+SPD_API spd_status kv_append_refresh(const spd_dims* dims, int32_t T, spd_bf16* K, spd_bf16* V,
+                                     const int32_t* page_table, const int32_t* seq_lens,
+                                     const spd_bf16* k_new, const spd_bf16* v_new, spd_bf16* summ,
+                                     void* stream) {
+    spd_status st = check_dims(dims);
+    if (st != SPD_OK) return st;
+    if (T < 1 || T > 4096) return fail(SPD_ERR_INVALID_ARG, "T = %d outside [1, 4096]", T);
+    if (dims->B == 0) return SPD_OK;
+    if (!K || !V || !page_table || !seq_lens || !k_new || !v_new || !summ)
+        return fail(SPD_ERR_INVALID_ARG, "NULL pointer argument");
+    if (!aligned16(K) || !aligned16(V) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(summ))
+        return fail(SPD_ERR_INVALID_ARG, "K, V, k_new, v_new and summ must be 16-byte aligned");
+    DevInfo* d = dev_info(&st);
+    if (!d) return st;
+    AppendArgs a;
+    a.K = K;
+    a.V = V;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.summ = summ;
+    a.B = dims->B;
+    a.T = T;
+    a.H_kv = dims->H_kv;
+    a.D = dims->D;
+    a.ps = dims->page_size;
+    a.max_pages = dims->max_pages_per_seq;
+    a.num_phys = dims->num_phys_pages;
+    a.status = d->status;
+    cudaError_t e = launch_append_refresh(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPD_OK : cuda_fail(e, "kv_append_refresh launch");
+}
+
 SPD_API spd_status pages_score_select(const spd_dims* dims, const spd_bf16* q, const spd_bf16* summ,
                                       const int32_t* seq_lens,
                                       const spd_budget_policy* policy, int32_t* sel, int32_t* nsel, int32_t k_max,

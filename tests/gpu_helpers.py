@@ -70,6 +70,15 @@ class Gpu:
                                    self.d["seq_lens"], o, ws, lse=lse, num_splits=num_splits)
         return o, lse, ws
 
+    def append(self, T, k_new, v_new, summ):
+        """kv_append_refresh on the device copies of K / V (k_new, v_new: numpy bf16 bits)."""
+        t = self.torch
+        kn = t.from_numpy(np.ascontiguousarray(k_new)).view(t.bfloat16).cuda()
+        vn = t.from_numpy(np.ascontiguousarray(v_new)).view(t.bfloat16).cuda()
+        self.spd.kv_append_refresh(self.dims, T, self.d["K"], self.d["V"], self.d["page_table"],
+                                   self.d["seq_lens"], kn, vn, summ)
+        return summ
+
     def sync_status(self):
         self.torch.cuda.synchronize()
         return self.spd.spd_device_status(clear=True)

@@ -67,6 +67,10 @@ def test_validation_rejects_bad_shapes_without_touching_the_gpu(libspd):
                                None, None, 0, None) == 2   # T = 0
     assert L.dense_verify_attn(ctypes.byref(d), 40, None, None, None, None, None, 0, 0.1, None,
                                None, None, 0, None) == 2   # T*G = 80 > 64
+    assert L.kv_append_refresh(ctypes.byref(d), 0, None, None, None, None, None, None, None,
+                               None) == 1                   # T = 0
+    assert L.kv_append_refresh(ctypes.byref(d), 1, None, None, None, None, None, None, None,
+                               None) == 1                   # NULL pointers
 
 
 def test_empty_batch_is_a_no_op(libspd):
