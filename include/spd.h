@@ -73,6 +73,7 @@ typedef enum {
 #define SPD_DEV_BAD_SEL 0x2u   /* a selected page id outside the sequence, or nsel > k_max */
 #define SPD_DEV_TIMEOUT 0x4u   /* a bounded wait on an asynchronous copy ran out */
 #define SPD_DEV_BAD_LEN 0x8u   /* kv_append_refresh: seq_lens[b] < T or beyond the page table */
+#define SPD_DEV_BAD_TOKEN 0x10u /* spec_accept: a drafted token outside [0, n_vocab) */
 
 /*
  * Problem shape.  Supported: D in {64, 128}; page_size in {16, 32, 64};
@@ -268,6 +269,38 @@ spd_status dense_verify_attn(const spd_dims *dims, int32_t T, const spd_bf16 *q,
                              const spd_bf16 *K, const spd_bf16 *V, const int32_t *page_table,
                              const int32_t *seq_lens, int32_t num_splits, float softmax_scale,
                              spd_bf16 *o, float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * spec_accept -- exact speculative sampling over k drafted tokens per sequence
+ * (S3R abstract: responses come from full-attention verification and exact
+ * speculative sampling, so they follow the dense policy; k = 6 in Table 7).
+ *
+ * p_draft fp32 [B][k][n_vocab]: the drafter's distribution at each drafted
+ * position; q_target fp32 [B][k+1][n_vocab]: the target's distribution at the
+ * same positions plus the one after the last draft (from dense_verify_attn's
+ * pass); draft int32 [B][k]; u_acc fp32 [B][k] and u_res fp32 [B]: uniform
+ * numbers in [0, 1) drawn by the caller.  Rows need not be normalised.
+ * For each sequence: draft x at position i is accepted iff
+ * u_acc[b][i] * p_i(x) < q_i(x) (product formed exactly in fp64), in order,
+ * until the first rejection j.  The emitted token is a draw from integer
+ * weights on a 2^-40 grid, W(x) = max(0, F(q_j(x)) - F(p_j(x))) with
+ * F(v) = floor(2^40 * min(v, 1)) (0 for v <= 0 or NaN), or W(x) = F(q_j(x))
+ * when that residual is zero everywhere; after k acceptances W(x) = F(q_k(x))
+ * (the bonus token).  The draw is the smallest x whose running sum of W
+ * exceeds floor(u_res[b] * sum(W)); all sums are exact integers, so the
+ * result does not depend on summation order.  W zero everywhere: -1.  (Mass
+ * below 2^-40 per token is never drawn: at most n_vocab * 2^-40 of total
+ * variation from the real-number rule.)
+ * Outputs: n_accepted int32 [B]; tokens int32 [B][k+1] = the accepted drafts,
+ * the emitted token, then -1.  A draft outside [0, n_vocab) at or before the
+ * first rejection sets SPD_DEV_BAD_TOKEN and gives that sequence
+ * n_accepted = 0, tokens = -1.
+ * Supported: 1 <= k <= 32, 1 <= n_vocab <= 2^21; p_draft and q_target 16-byte
+ * aligned.
+ */
+spd_status spec_accept(int32_t B, int32_t k, int32_t n_vocab, const float *p_draft,
+                       const float *q_target, const int32_t *draft, const float *u_acc,
+                       const float *u_res, int32_t *n_accepted, int32_t *tokens, void *stream);
 
 /*
  * lse_merge -- combine S partial attention results computed over disjoint

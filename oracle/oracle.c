@@ -372,23 +372,40 @@ void oracle_append_seq(int T, int H_kv, int D, int ps, int max_pages, uint16_t *
 }
 
 /*
- * A draw from the unnormalised weights w[0..n) with a uniform u in [0, 1):
- * the smallest x whose running sum exceeds u * sum(w).  If rounding leaves
- * no such x, the last x with w[x] > 0.  All weights zero: -1.
+ * Weight of a probability in the draw: floor(2^40 * v), exactly (scaling a
+ * float by a power of two is exact and the conversion truncates).  Values at
+ * or above 1 count as 1; zero, negative and NaN values count as 0.
  */
-static int draw(const double *w, int n, double u)
+static uint64_t fixed40(float v)
 {
-    double total = 0.0;
-    for (int x = 0; x < n; ++x) total += w[x];
-    if (!(total > 0.0)) return -1;
-    double target = u * total, run = 0.0;
-    int last = -1;
+    if (!(v > 0.0f)) return 0;
+    if (v >= 1.0f) return (uint64_t)1 << 40;
+    return (uint64_t)(v * 0x1p40f);
+}
+
+/*
+ * A draw from integer weights W[0..n) with a uniform float u in [0, 1): the
+ * smallest x whose running sum exceeds T = floor(u * sum(W)), all in exact
+ * integer arithmetic (u = m * 2^e with an integer m; the product m * sum(W)
+ * needs 128 bits).  All weights zero: -1.
+ */
+static int draw_fixed(const uint64_t *W, int n, float u)
+{
+    uint64_t total = 0;
+    for (int x = 0; x < n; ++x) total += W[x];
+    if (total == 0) return -1;
+    int e;
+    double fr = frexp((double)u, &e);           /* u = fr * 2^e, fr in [0.5, 1) */
+    uint64_t m = (uint64_t)ldexp(fr, 24);       /* exact: u has 24 significant bits */
+    int shift = 24 - e;                         /* u = m * 2^-shift */
+    unsigned __int128 prod = (unsigned __int128)m * total;
+    uint64_t target = shift >= 128 ? 0 : (uint64_t)(prod >> shift);
+    uint64_t run = 0;
     for (int x = 0; x < n; ++x) {
-        if (w[x] > 0.0) last = x;
-        run += w[x];
+        run += W[x];
         if (run > target) return x;
     }
-    return last;
+    return -1; /* not reached: target < total for u < 1 */
 }
 
 /*
@@ -397,14 +414,19 @@ static int draw(const double *w, int n, double u)
  * follow the dense policy).  The rule is the standard one for a drafter
  * distribution p and a target distribution q over a vocabulary of n tokens:
  *   for i = 0 .. k-1, with x = draft[i]: accept iff u_acc[i] * p_i(x) < q_i(x)
- *   (accept with probability min(1, q_i(x) / p_i(x)));
- *   at the first rejection j, emit a draw (u_res) from max(0, q_j - p_j), or
- *   from q_j when that residual is zero everywhere;
+ *   (accept with probability min(1, q_i(x) / p_i(x))), the product of the two
+ *   floats formed exactly in double;
+ *   at the first rejection j, emit a draw (u_res) from the residual
+ *   max(0, q_j - p_j), or from q_j when the residual is zero everywhere;
  *   if all k drafts are accepted, emit a bonus draw (u_res) from q_k.
- * p is [k][n] and q is [k+1][n] (fp32 probabilities, widened exactly; the
- * products u * p of two fp32 values are exact in double).  tokens[0..k]
- * receives the accepted drafts then the emitted token, -1 after it; the
- * return value is the number of accepted drafts.
+ * The draw's weights are probabilities on a grid of 2^-40, so that every sum
+ * is exact and independent of order: the residual weight of x is
+ * max(0, floor(2^40 q(x)) - floor(2^40 p(x))), the plain weight
+ * floor(2^40 q(x)).  (Tokens below 2^-40 of mass are never drawn: a total
+ * variation of at most n * 2^-40 from the exact rule.)
+ * p is [k][n] and q is [k+1][n] fp32.  tokens[0..k] receives the accepted
+ * drafts then the emitted token, -1 after it; the return value is the number
+ * of accepted drafts.
  */
 int oracle_spec_accept_seq(int k, int n, const float *p, const float *q, const int32_t *draft,
                            const float *u_acc, float u_res, int32_t *tokens)
@@ -417,25 +439,22 @@ int oracle_spec_accept_seq(int k, int n, const float *p, const float *q, const i
         tokens[acc] = x;
         ++acc;
     }
-    double *w = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    uint64_t *W = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(n > 0 ? n : 1));
     const float *qr = q + (size_t)acc * n;
-    int tok;
+    int tok = -1;
     if (acc < k) {
         const float *pr = p + (size_t)acc * n;
         for (int x = 0; x < n; ++x) {
-            double r = (double)qr[x] - (double)pr[x];
-            w[x] = r > 0.0 ? r : 0.0;
+            uint64_t a = fixed40(qr[x]), b = fixed40(pr[x]);
+            W[x] = a > b ? a - b : 0;
         }
-        tok = draw(w, n, (double)u_res);
-        if (tok < 0) {
-            for (int x = 0; x < n; ++x) w[x] = qr[x] > 0.f ? (double)qr[x] : 0.0;
-            tok = draw(w, n, (double)u_res);
-        }
-    } else {
-        for (int x = 0; x < n; ++x) w[x] = qr[x] > 0.f ? (double)qr[x] : 0.0;
-        tok = draw(w, n, (double)u_res);
+        tok = draw_fixed(W, n, u_res);
     }
-    free(w);
+    if (tok < 0) {
+        for (int x = 0; x < n; ++x) W[x] = fixed40(qr[x]);
+        tok = draw_fixed(W, n, u_res);
+    }
+    free(W);
     tokens[acc] = tok;
     for (int i = acc + 1; i <= k; ++i) tokens[i] = -1;
     return acc;
