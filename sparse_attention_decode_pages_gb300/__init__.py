@@ -84,9 +84,10 @@ def lib():
                                                  P, P, P]
         L.lse_merge.argtypes = [i32, i32, i32, P, P, P, P, P]
         L.kv_append_refresh.argtypes = [DP, i32, P, P, P, P, P, P, P, P]
+        L.spec_accept.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, P]
         for f in ("spd_device_status", "pages_summarize", "pages_score_select",
                   "sparse_decode_attn", "dense_verify_attn", "lse_merge",
-                  "sparse_decode_attn_noalloc", "kv_append_refresh"):
+                  "sparse_decode_attn_noalloc", "kv_append_refresh", "spec_accept"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -167,6 +168,13 @@ def kv_append_refresh(dims: Dims, T: int, K, V, page_table, seq_lens, k_new, v_n
     _check(lib().kv_append_refresh(ctypes.byref(dims), T, _ptr(K), _ptr(V), _ptr(page_table),
                                    _ptr(seq_lens), _ptr(k_new), _ptr(v_new), _ptr(summ),
                                    _stream(stream)))
+
+
+def spec_accept(p_draft, q_target, draft, u_acc, u_res, n_accepted, tokens, stream=None):
+    """p_draft [B][k][n], q_target [B][k+1][n] (fp32), draft int32 [B][k], u_acc [B][k], u_res [B]."""
+    B, k, n = p_draft.shape
+    _check(lib().spec_accept(B, k, n, _ptr(p_draft), _ptr(q_target), _ptr(draft), _ptr(u_acc),
+                             _ptr(u_res), _ptr(n_accepted), _ptr(tokens), _stream(stream)))
 
 
 def pages_score_select(dims: Dims, q, summ, seq_lens, policy, sel, nsel, k_max: int, ws,

@@ -37,6 +37,21 @@ struct AppendArgs {
 };
 cudaError_t launch_append_refresh(const AppendArgs& a, cudaStream_t st);
 
+struct SpecArgs {
+    const float* p;        // [B][k][n] drafter probabilities
+    const float* q;        // [B][k+1][n] target probabilities
+    const int32_t* draft;  // [B][k]
+    const float* u_acc;    // [B][k]
+    const float* u_res;    // [B]
+    int32_t* n_accepted;   // [B]
+    int32_t* tokens;       // [B][k+1]
+    int B, k;
+    long long n;
+    unsigned* status;
+};
+cudaError_t launch_spec_accept(const SpecArgs& a, cudaStream_t st);
+size_t spec_smem_bytes(long long n);
+
 struct ScoreSelectArgs {
     const uint16_t* q;
     const uint16_t* summ;  // [B][H_kv][max_pages][2][D]

@@ -310,6 +310,36 @@ SPD_API spd_status kv_append_refresh(const spd_dims* dims, int32_t T, spd_bf16* 
     return e == cudaSuccess ? SPD_OK : cuda_fail(e, "kv_append_refresh launch");
 }
 
+SPD_API spd_status spec_accept(int32_t B, int32_t k, int32_t n_vocab, const float* p_draft,
+                               const float* q_target, const int32_t* draft, const float* u_acc,
+                               const float* u_res, int32_t* n_accepted, int32_t* tokens, void* stream) {
+    if (B < 0) return fail(SPD_ERR_INVALID_ARG, "B < 0");
+    if (k < 1 || k > 32) return fail(SPD_ERR_UNSUPPORTED, "k = %d outside [1, 32]", k);
+    if (n_vocab < 1 || n_vocab > (1 << 21)) return fail(SPD_ERR_UNSUPPORTED, "n_vocab = %d outside [1, 2^21]", n_vocab);
+    if (B == 0) return SPD_OK;
+    if (!p_draft || !q_target || !draft || !u_acc || !u_res || !n_accepted || !tokens)
+        return fail(SPD_ERR_INVALID_ARG, "NULL pointer argument");
+    if (!aligned16(p_draft) || !aligned16(q_target))
+        return fail(SPD_ERR_INVALID_ARG, "p_draft and q_target must be 16-byte aligned");
+    spd_status st;
+    DevInfo* d = dev_info(&st);
+    if (!d) return st;
+    SpecArgs a;
+    a.p = p_draft;
+    a.q = q_target;
+    a.draft = draft;
+    a.u_acc = u_acc;
+    a.u_res = u_res;
+    a.n_accepted = n_accepted;
+    a.tokens = tokens;
+    a.B = B;
+    a.k = k;
+    a.n = n_vocab;
+    a.status = d->status;
+    cudaError_t e = launch_spec_accept(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPD_OK : cuda_fail(e, "spec_accept launch");
+}
+
 SPD_API spd_status pages_score_select(const spd_dims* dims, const spd_bf16* q, const spd_bf16* summ,
                                       const int32_t* seq_lens,
                                       const spd_budget_policy* policy, int32_t* sel, int32_t* nsel, int32_t k_max,

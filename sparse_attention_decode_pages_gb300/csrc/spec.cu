@@ -1,0 +1,302 @@
+// spec.cu -- exact speculative sampling after dense verification: the
+// accept / reject decisions over k drafted tokens and the draw of the token
+// that follows them (S3R abstract: responses come from full-attention
+// verification followed by exact speculative sampling).
+//
+// One cluster of kSpecCluster CTAs per sequence.  Each CTA's first warp
+// decides the k drafts at once, a lane each (cheap; every CTA needs the
+// outcome): draft x at position i is accepted iff u_acc * p_i(x) < q_i(x),
+// the product of the two fp32 values formed exactly in fp64; the first
+// rejection ends the run.
+//
+// The token that follows is drawn from integer weights on a 2^-40 grid:
+// W(x) = max(0, F(q_j(x)) - F(p_j(x))) at the first rejection j (F(q_j(x))
+// when that is zero everywhere), or F(q_k(x)) after k acceptances, with
+// F(v) = floor(2^40 v).  The draw is the smallest x whose running sum exceeds
+// floor(u_res * sum W).  Every sum is an exact 64-bit integer, so the order in
+// which the GPU adds them does not matter (fp64 would be both order-dependent
+// and slow: this part runs fp64 at a small fraction of its fp32 rate).
+//
+// The draw streams the row once.  Each CTA sums the 128-element tiles of its
+// share of the row, a warp per tile and two tiles in flight per warp, into its
+// shared memory.  After a cluster barrier, CTA 0 gathers every tile sum
+// through distributed shared memory and block-scans contiguous runs of them;
+// the one thread whose run holds the target finds the crossing tile, and a
+// warp scans that tile's 128 weights to find the element.
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace cg = cooperative_groups;
+
+namespace spd {
+
+constexpr int kSpecThreads = 512;
+constexpr int kSpecTile = 128;
+constexpr int kSpecCluster = 8;
+constexpr int kSpecUnroll = 2;
+typedef unsigned long long u64;
+
+// floor(2^40 v) from the float's bits, in integer operations only (a 64-bit
+// float-to-integer conversion is a slow instruction): for a normal v < 1,
+// v = mant * 2^(E - 150), so 2^40 v = (mant << 40) >> (150 - E), a shift the
+// PTX shr clamps to 0 past 64.  v >= 1 (and +inf) counts as 1; v <= 0, NaN and
+// subnormals (far below the grid) give 0.
+__device__ __forceinline__ u64 fixed40(float v) {
+    const unsigned bits = __float_as_uint(v);
+    const unsigned E = bits >> 23;  // with the sign bit: negative values give E >= 256
+    const u64 x = (u64)((bits & 0x7fffffu) | 0x800000u) << 40;
+    u64 w;
+    asm("shr.b64 %0, %1, %2;" : "=l"(w) : "l"(x), "r"(150u - E));
+    if (E - 1u >= 126u) {  // not a normal value in (0, 1)
+        const bool one = E >= 127u && E <= 255u && !(E == 255u && (bits & 0x7fffffu));
+        w = one ? (1ull << 40) : 0ull;
+    }
+    return w;
+}
+
+__device__ __forceinline__ u64 spec_w(float qv, float pv, bool residual) {
+    const u64 a = fixed40(qv);
+    if (!residual) return a;
+    const u64 b = fixed40(pv);
+    return a > b ? a - b : 0ull;
+}
+
+// floor(u * total) for a float u in [0, 1), exactly: u = m * 2^-shift
+__device__ __forceinline__ u64 scaled_floor(float u, u64 total) {
+    const unsigned bits = __float_as_uint(u);
+    const unsigned E = (bits >> 23) & 0xffu;
+    u64 m;
+    int shift;
+    if (E == 0) {
+        m = bits & 0x7fffffu;
+        shift = 149;
+    } else {
+        m = (bits & 0x7fffffu) | 0x800000u;
+        shift = 150 - (int)E;
+    }
+    if (shift <= 0) return ~0ull;  // u >= 2^23: past any total
+    const u64 lo = m * total, hi = __umul64hi(m, total);
+    if (shift >= 128) return 0ull;
+    if (shift >= 64) return hi >> (shift - 64);
+    return (lo >> shift) | (hi << (64 - shift));
+}
+
+__device__ __forceinline__ u64 shfl_xor_u64(u64 v, int off) {
+    return __shfl_xor_sync(0xffffffffu, v, off);
+}
+
+template <bool VEC>
+__global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThreads, 2)
+    spec_accept_kernel(SpecArgs a) {
+    extern __shared__ u64 smem_w[];  // [tpc] own tile sums, then (CTA 0) [ntiles] all tile sums
+    __shared__ int s_acc, s_bad, s_tok, s_cross_tile;
+    __shared__ u64 s_cross_run;
+    __shared__ u64 s_warp[kSpecThreads / 32];
+    __shared__ u64 s_chunk;  // this CTA's share of the total
+    constexpr int NW = kSpecThreads / 32;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x / kSpecCluster;
+    const int k = a.k;
+    const long long n = a.n;
+    const int ntiles = (int)((n + kSpecTile - 1) / kSpecTile);
+    const int tpc = (ntiles + kSpecCluster - 1) / kSpecCluster;  // tiles per CTA
+    u64* tsum = smem_w;
+    u64* all = smem_w + tpc;
+
+    // the k <= 32 decisions in parallel, one lane each; the first rejection ends the run
+    if (warp == 0) {
+        bool ok = false, bad = false;
+        if (lane < k) {
+            const int x = a.draft[(long long)b * k + lane];
+            if (x < 0 || x >= n) {
+                bad = true;
+            } else {
+                const double px = (double)a.p[((long long)b * k + lane) * n + x];
+                const double qx = (double)a.q[((long long)b * (k + 1) + lane) * n + x];
+                ok = (double)a.u_acc[(long long)b * k + lane] * px < qx;
+            }
+        }
+        const unsigned fail = __ballot_sync(0xffffffffu, lane < k && !ok);
+        const unsigned badm = __ballot_sync(0xffffffffu, bad);
+        if (lane == 0) {
+            const int j = fail ? __ffs((int)fail) - 1 : k;
+            // a bad token at the first failing position invalidates the sequence
+            s_acc = j;
+            s_bad = (j < k && ((badm >> j) & 1u)) ? 1 : 0;
+            s_tok = -1;
+            if (s_bad && rank == 0) raise_status(a.status, SPD_DEV_BAD_TOKEN);
+        }
+    }
+    __syncthreads();
+    const int acc = s_acc;
+    int32_t* out = a.tokens + (long long)b * (k + 1);
+    if (s_bad) {  // the same on every CTA of the cluster: all leave before any barrier
+        if (rank == 0) {
+            for (int i = tid; i <= k; i += kSpecThreads) out[i] = -1;
+            if (tid == 0) a.n_accepted[b] = 0;
+        }
+        return;
+    }
+    const float* qr = a.q + ((long long)b * (k + 1) + acc) * n;
+    const float* pr = acc < k ? a.p + ((long long)b * k + acc) * n : qr;
+    const int my0 = rank * tpc;
+    const int my1 = min(ntiles, my0 + tpc);
+
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        // attempt 0: the residual at a rejection, or the target row after k acceptances;
+        // attempt 1 (after a rejection whose residual is zero everywhere): the target row
+        const bool residual = (attempt == 0) && (acc < k);
+        for (int t = my0 + warp; t < my1; t += NW * kSpecUnroll) {
+            float4 q4[kSpecUnroll], p4[kSpecUnroll];
+#pragma unroll
+            for (int u = 0; u < kSpecUnroll; ++u) {
+                const int tt = t + u * NW;
+                const long long x0 = (long long)tt * kSpecTile + lane * 4;
+                q4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                p4[u] = q4[u];
+                if (tt < my1) {
+                    if (VEC && x0 + 4 <= n) {
+                        q4[u] = __ldg(reinterpret_cast<const float4*>(qr + x0));
+                        if (residual) p4[u] = __ldg(reinterpret_cast<const float4*>(pr + x0));
+                    } else {
+                        float qv[4] = {0.f, 0.f, 0.f, 0.f}, pv[4] = {0.f, 0.f, 0.f, 0.f};
+                        for (int j = 0; j < 4 && x0 + j < n; ++j) {
+                            qv[j] = __ldg(qr + x0 + j);
+                            if (residual) pv[j] = __ldg(pr + x0 + j);
+                        }
+                        q4[u] = make_float4(qv[0], qv[1], qv[2], qv[3]);
+                        p4[u] = make_float4(pv[0], pv[1], pv[2], pv[3]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kSpecUnroll; ++u) {
+                const int tt = t + u * NW;
+                if (tt >= my1) break;  // warp-uniform
+                u64 s = spec_w(q4[u].x, p4[u].x, residual) + spec_w(q4[u].y, p4[u].y, residual) +
+                        spec_w(q4[u].z, p4[u].z, residual) + spec_w(q4[u].w, p4[u].w, residual);
+#pragma unroll
+                for (int off = 16; off; off >>= 1) s += shfl_xor_u64(s, off);
+                if (lane == 0) tsum[tt - my0] = s;
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {
+            u64 c = 0;
+            for (int t = lane; t < my1 - my0; t += 32) c += tsum[t];
+#pragma unroll
+            for (int off = 16; off; off >>= 1) c += shfl_xor_u64(c, off);
+            if (lane == 0) s_chunk = c;
+        }
+        cluster.sync();  // every CTA's tile sums and share are visible cluster-wide
+        u64 total = 0;
+        for (int r = 0; r < kSpecCluster; ++r) total += *cluster.map_shared_rank(&s_chunk, r);
+        if (total == 0) {
+            cluster.sync();  // nobody reads this attempt's sums any more
+            if (acc == k) break;  // the target row itself is zero: no token
+            continue;
+        }
+        if (rank == 0) {
+            if (tid == 0) s_cross_tile = -1;
+            for (int t = tid; t < ntiles; t += kSpecThreads) {
+                const int r = t / tpc;
+                all[t] = cluster.map_shared_rank(tsum, r)[t - r * tpc];
+            }
+            __syncthreads();
+            const u64 target = scaled_floor(a.u_res[b], total);
+            const int per = (ntiles + kSpecThreads - 1) / kSpecThreads;
+            const int t0 = tid * per;
+            const int t1 = min(ntiles, t0 + per);
+            u64 mine = 0;
+            for (int t = t0; t < t1; ++t) mine += all[t];
+            u64 incl = mine;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const u64 y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            if (lane == 31) s_warp[warp] = incl;
+            __syncthreads();
+            u64 before = 0;
+            for (int w = 0; w < warp; ++w) before += s_warp[w];
+            const u64 excl = before + incl - mine;
+            if (excl <= target && target < excl + mine) {
+                // the crossing lies in this thread's run: find its tile from the sums
+                u64 run = excl;
+                int t = t0;
+                for (; t < t1 - 1; ++t) {
+                    if (run + all[t] > target) break;
+                    run += all[t];
+                }
+                s_cross_tile = t;
+                s_cross_run = run;
+            }
+            __syncthreads();
+            if (warp == 0 && s_cross_tile >= 0) {
+                // the tile's 128 weights: 4 per lane, a warp scan of the lane sums
+                const long long x0 = (long long)s_cross_tile * kSpecTile + lane * 4;
+                u64 w[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    w[j] = (x0 + j < n) ? spec_w(__ldg(qr + x0 + j), residual ? __ldg(pr + x0 + j) : 0.f, residual) : 0ull;
+                const u64 lsum = w[0] + w[1] + w[2] + w[3];
+                u64 incl_l = lsum;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const u64 y = __shfl_up_sync(0xffffffffu, incl_l, off);
+                    if (lane >= off) incl_l += y;
+                }
+                u64 r = s_cross_run + (incl_l - lsum);
+                int hit = -1;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    r += w[j];
+                    if (hit < 0 && r > target) hit = (int)(x0 + j);
+                }
+                const unsigned m = __ballot_sync(0xffffffffu, hit >= 0);
+                if (m && lane == __ffs((int)m) - 1) s_tok = hit;
+            }
+        }
+        cluster.sync();  // CTA 0 is done reading the others' shared memory
+        break;
+    }
+    if (rank == 0) {
+        __syncthreads();
+        for (int i = tid; i <= k; i += kSpecThreads) {
+            if (i < acc)
+                out[i] = a.draft[(long long)b * k + i];
+            else
+                out[i] = (i == acc) ? s_tok : -1;
+        }
+        if (tid == 0) a.n_accepted[b] = acc;
+    }
+}
+
+size_t spec_smem_bytes(long long n) {
+    const long long ntiles = (n + kSpecTile - 1) / kSpecTile;
+    const long long tpc = (ntiles + kSpecCluster - 1) / kSpecCluster;
+    return (size_t)(tpc + ntiles) * sizeof(u64);
+}
+
+cudaError_t launch_spec_accept(const SpecArgs& a, cudaStream_t st) {
+    if (a.B <= 0) return cudaSuccess;
+    const size_t smem = spec_smem_bytes(a.n);
+    const unsigned grid = (unsigned)a.B * kSpecCluster;
+    cudaError_t e;
+    if (a.n % 4 == 0) {
+        e = cudaFuncSetAttribute(spec_accept_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        spec_accept_kernel<true><<<grid, kSpecThreads, smem, st>>>(a);
+    } else {
+        e = cudaFuncSetAttribute(spec_accept_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        spec_accept_kernel<false><<<grid, kSpecThreads, smem, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace spd

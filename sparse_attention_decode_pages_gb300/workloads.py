@@ -40,6 +40,14 @@ the order above; the sweep adds the page size to the seed):
 
 Large arrays are generated in fixed chunks, each with its own child seed, so
 the bytes do not depend on how many threads generate them.
+
+Speculative-sampling inputs (``spec_inputs``; S3R Table 7: k = 6 drafts per
+round, Qwen3's 151,936-token vocabulary): each drafter row p_i is a Dirichlet
+draw with concentration 0.05 per token (peaked, like a sampled LM
+distribution); each target row is (1 - eps) * p_i + eps * (an independent
+Dirichlet draw), eps = 0.3, and the row after the last draft is a fresh
+Dirichlet draw.  Drafted tokens are drawn from p_i; the uniform numbers are
+float32 draws in [0, 1).  Seed 1006.
 """
 from __future__ import annotations
 
@@ -311,3 +319,36 @@ def to_device(w: Workload, device="cuda") -> dict:
     if w.q_verify is not None:
         out["q_verify"] = bf(w.q_verify)
     return out
+
+
+VOCAB_QWEN3 = 151936
+
+
+def _dirichlet_rows(rng, rows: int, n: int, alpha: float) -> np.ndarray:
+    g = rng.standard_gamma(alpha, size=(rows, n))
+    g /= g.sum(axis=1, keepdims=True)
+    return g
+
+
+def spec_inputs(B: int = 64, k: int = 6, n: int = VOCAB_QWEN3, seed: int = 1006,
+                alpha: float = 0.05, eps: float = 0.3) -> dict:
+    """Seeded drafter / target probability rows and the random numbers of one round.
+
+    Returns p float32 [B][k][n], q float32 [B][k+1][n], draft int32 [B][k], u_acc
+    float32 [B][k], u_res float32 [B]."""
+    rng = np.random.default_rng(seed)
+    p = np.empty((B, k, n), np.float32)
+    q = np.empty((B, k + 1, n), np.float32)
+    draft = np.empty((B, k), np.int32)
+    for b in range(B):
+        pb = _dirichlet_rows(rng, k, n, alpha)
+        mix = _dirichlet_rows(rng, k + 1, n, alpha)
+        p[b] = pb
+        q[b, :k] = (1.0 - eps) * pb + eps * mix[:k]
+        q[b, k] = mix[k]
+        c = np.cumsum(pb, axis=1)
+        u = rng.random(k)
+        draft[b] = np.minimum([np.searchsorted(c[i], u[i] * c[i, -1], side="right") for i in range(k)], n - 1)
+    u_acc = rng.random((B, k), dtype=np.float32)
+    u_res = rng.random(B, dtype=np.float32)
+    return dict(p=p, q=q, draft=draft, u_acc=u_acc, u_res=u_res)

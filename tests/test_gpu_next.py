@@ -102,3 +102,77 @@ def test_append_then_decode_matches_oracle_pipeline():
     rows = [b for b in range(w.B) if all((b, h) in same for h in range(w.H_kv))]
     assert rows
     assert_close_outputs(np_bf16(o)[rows], ref["o"][rows], lse.cpu().numpy()[rows], ref["lse"][rows])
+
+
+# ---------------------------------------------------------------- f2 speculative sampling
+
+def _spec_gpu(p, q, draft, u_acc, u_res):
+    import torch
+    import sparse_attention_decode_pages_gb300 as spd
+    dev = "cuda"
+    P = torch.from_numpy(np.ascontiguousarray(p, np.float32)).to(dev)
+    Q = torch.from_numpy(np.ascontiguousarray(q, np.float32)).to(dev)
+    Dr = torch.from_numpy(np.ascontiguousarray(draft, np.int32)).to(dev)
+    Ua = torch.from_numpy(np.ascontiguousarray(u_acc, np.float32)).to(dev)
+    Ur = torch.from_numpy(np.ascontiguousarray(u_res, np.float32)).to(dev)
+    B, k, n = p.shape
+    nacc = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    toks = torch.full((B, k + 1), -7, dtype=torch.int32, device=dev)
+    spd.spec_accept(P, Q, Dr, Ua, Ur, nacc, toks)
+    torch.cuda.synchronize()
+    return nacc.cpu().numpy(), toks.cpu().numpy(), spd.spd_device_status(clear=True)
+
+
+def _compare_spec(d):
+    """Accept counts and tokens bit-identical to the oracle (the draw is exact integer
+    arithmetic on both sides)."""
+    import oracle as orc
+    na_r, tk_r = orc.spec_accept(d["p"], d["q"], d["draft"], d["u_acc"], d["u_res"])
+    na_g, tk_g, st = _spec_gpu(d["p"], d["q"], d["draft"], d["u_acc"], d["u_res"])
+    assert st == 0, st
+    assert np.array_equal(na_g, na_r)
+    assert np.array_equal(tk_g, tk_r), np.argwhere(tk_g != tk_r)[:5]
+    return na_r
+
+
+def test_spec_accept_hand_worked_cases_on_gpu():
+    from tests.test_oracle_pins_next import _golden_spec
+    for k, n, p, q, draft, uacc, ures, nacc, toks in _golden_spec():
+        na, tk, st = _spec_gpu(p[None], q[None], np.array([draft]), np.array([uacc], np.float32),
+                               np.array([ures], np.float32))
+        assert st == 0 and na[0] == nacc and tk[0].tolist() == toks, (k, n, na, tk)
+
+
+@pytest.mark.parametrize("n", [1000, 4099, 151936])
+def test_spec_accept_matches_oracle(n):
+    d = wl.spec_inputs(B=24, k=6, n=n, seed=77 + n)
+    nacc = _compare_spec(d)
+    assert nacc.min() < 6 and nacc.max() > 0     # both rejections and acceptances occur
+
+
+def test_spec_accept_all_accepted_zero_residual_and_empty_rows():
+    rng = np.random.default_rng(5)
+    n, k, B = 4096, 6, 6
+    p = rng.random((B, k, n)).astype(np.float32)
+    q = np.concatenate([p, rng.random((B, 1, n)).astype(np.float32)], axis=1)
+    draft = rng.integers(0, n, size=(B, k)).astype(np.int32)
+    u_acc = (rng.random((B, k)) * 0.999).astype(np.float32)
+    # row 1: target = drafter / 2 at position 2, rejected there with a zero residual
+    q[1, 2] = p[1, 2] * 0.5
+    u_acc[1, 2] = 0.75
+    # row 2: the bonus row is all zero -> no token
+    q[2, k] = 0.0
+    # row 3: rejected at 0 with residual and target both zero -> no token
+    q[3, 0] = 0.0
+    d = dict(p=p, q=q, draft=draft, u_acc=u_acc, u_res=rng.random(B, dtype=np.float32))
+    nacc = _compare_spec(d)
+    assert nacc.tolist() == [6, 2, 6, 0, 6, 6]
+    na_g, tk_g, _ = _spec_gpu(p, q, draft, u_acc, d["u_res"])
+    assert tk_g[2, k] == -1 and tk_g[3, 0] == -1
+
+
+def test_spec_accept_bad_draft_token_sets_status():
+    d = wl.spec_inputs(B=3, k=2, n=512, seed=3)
+    d["draft"][1, 1] = 512
+    na, tk, st = _spec_gpu(d["p"], d["q"], d["draft"], d["u_acc"], d["u_res"])
+    assert st == 0x10 and na[1] == 0 and np.all(tk[1] == -1)
