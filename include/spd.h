@@ -93,7 +93,8 @@ typedef struct {
 typedef enum {
     SPD_BUDGET_FIXED_PAGES = 0,   /* budget = fixed_pages */
     SPD_BUDGET_LINEAR_TOKENS = 1, /* ceil(max(min_tokens, ceil(len*slope_num/slope_den) + intercept) / page_size) */
-    SPD_BUDGET_FRACTION = 2       /* ceil(len * frac_num / (frac_den * page_size)) */
+    SPD_BUDGET_FRACTION = 2,      /* ceil(len * frac_num / (frac_den * page_size)) */
+    SPD_BUDGET_TOP_P = 3          /* the smallest set holding top_p of the page weight (below) */
 } spd_budget_mode;
 
 /*
@@ -103,6 +104,17 @@ typedef enum {
  * local window) are always selected and count toward the budget.  The number
  * of pages selected for a (sequence, KV head) is
  *   k_eff = min(P, max(min(budget, k_max), |mandatory|)),  P = ceil(len / page_size).
+ *
+ * SPD_BUDGET_TOP_P makes the budget query-dependent (the pages stress that the
+ * budget a query needs varies strongly: S3R abstract, Sparrow "Control Study
+ * 1").  Each page gets the weight w(p) = exp(score_scale * (score(p) - max
+ * score)), a softmax over pages of the bound logits; after the mandatory
+ * pages, the best-scoring pages are added until the selected weight reaches
+ * top_p of the total, at most k_max pages in all.  On the device the weights
+ * are fp32 exponentials rounded to multiples of 2^-31 and summed as exact
+ * integers, so the count is deterministic; it can differ from a real-number
+ * evaluation only where the selected weight lands within that rounding of
+ * the top_p share.
  */
 typedef struct {
     int32_t mode; /* spd_budget_mode */
@@ -110,6 +122,8 @@ typedef struct {
     int64_t min_tokens, slope_num, slope_den, intercept; /* LINEAR_TOKENS (slope_den > 0) */
     int64_t frac_num, frac_den;                          /* FRACTION (frac_den > 0) */
     int32_t sink_pages, local_pages;                     /* >= 0 */
+    float top_p;       /* TOP_P: share of the page weight to hold, in [0, 1] */
+    float score_scale; /* TOP_P: logit scale of the scores (> 0), e.g. 1 / sqrt(D) */
 } spd_budget_policy;
 
 /* Library ABI version (major * 100 + minor). */

@@ -132,8 +132,11 @@ def k_eff(pol, length: int, page_size: int, k_max: int) -> int:
 
 def select(w, sc, policy=None, k_max=None, seqs=None, threads=None):
     """Step a4: (sel int32 [B][H_kv][k_max], nsel int32 [B][H_kv]); unused slots are -1."""
-    L = lib()
     pol = w.policy if policy is None else policy
+    if pol.mode == "top_p":
+        return select_top_p(w, sc, pol.top_p, pol.score_scale, k_max=k_max, policy=pol, seqs=seqs,
+                            threads=threads)
+    L = lib()
     k_max = w.k_max if k_max is None else k_max
     m, a, b_, c, d = _policy_args(pol)
     sel = np.full((w.B, w.H_kv, k_max), -1, dtype=np.int32)

@@ -30,7 +30,7 @@ LIB_PATH = os.path.join(_HERE, "libspd.so")
 
 DEV_BAD_PAGE, DEV_BAD_SEL, DEV_TIMEOUT = 0x1, 0x2, 0x4
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "WORKSPACE"}
-_MODES = {"fixed": 0, "linear": 1, "fraction": 2}
+_MODES = {"fixed": 0, "linear": 1, "fraction": 2, "top_p": 3}
 
 
 class SpdError(RuntimeError):
@@ -50,7 +50,8 @@ class Policy(ctypes.Structure):
                 ("min_tokens", ctypes.c_int64), ("slope_num", ctypes.c_int64),
                 ("slope_den", ctypes.c_int64), ("intercept", ctypes.c_int64),
                 ("frac_num", ctypes.c_int64), ("frac_den", ctypes.c_int64),
-                ("sink_pages", ctypes.c_int32), ("local_pages", ctypes.c_int32)]
+                ("sink_pages", ctypes.c_int32), ("local_pages", ctypes.c_int32),
+                ("top_p", ctypes.c_float), ("score_scale", ctypes.c_float)]
 
 
 _lib = None
@@ -122,7 +123,8 @@ def policy_of(p) -> Policy:
     """A ``Policy`` from any object with the fields of ``workloads.BudgetPolicy``."""
     return Policy(_MODES[p.mode] if isinstance(p.mode, str) else int(p.mode), p.fixed_pages,
                   p.min_tokens, p.slope_num, p.slope_den, p.intercept, p.frac_num, p.frac_den,
-                  p.sink_pages, p.local_pages)
+                  p.sink_pages, p.local_pages, float(getattr(p, "top_p", 0.0)),
+                  float(getattr(p, "score_scale", 0.0)))
 
 
 def _size(v: int, what: str) -> int:

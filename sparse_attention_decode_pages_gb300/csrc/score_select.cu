@@ -59,6 +59,141 @@ __device__ __forceinline__ long long budget_pages(const spd_budget_policy& pol, 
 constexpr int kSelWarps = 8;
 constexpr int kSelThreads = 32 * kSelWarps;
 
+__device__ __forceinline__ float key_float(uint32_t u) {
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+
+// Page weight on a 2^-31 grid: exp(score_scale * (score - max)) * 2^31, rounded.
+__device__ __forceinline__ uint32_t page_weight(uint32_t key, float smax, float c2) {
+    const float w = exp2f((key_float(key) - smax) * c2);
+    return __float2uint_rn(w * 2147483648.0f);
+}
+
+__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, unsigned long long* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    unsigned long long t = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+    return t;
+}
+
+// Query-dependent budget: the number of non-mandatory pages that, taken in
+// score order after the mandatory ones, bring the selected page weight to
+// top_p of the total (all of them if none does).  Weights are integers on a
+// 2^-31 grid, so every sum is exact.  The k'-th page is found by an 8-bit radix
+// descent over the keys in which each bin carries its count and its weight.
+template <class Mand>
+__device__ int top_p_pages(const ScoreSelectArgs& a, const uint32_t* keys, int P, Mand mand,
+                           uint32_t* hist, int& s_digit, int& s_rem) {
+    typedef unsigned long long u64;
+    __shared__ u64 mhist[256];
+    __shared__ u64 red[kSelWarps];
+    __shared__ u64 s_mass;
+    __shared__ uint32_t s_kmax;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ncand = P - min(P, min(a.pol.sink_pages, P) + min(a.pol.local_pages, P));
+    if (tid == 0) s_kmax = 0;
+    __syncthreads();
+    uint32_t km = 0;
+    for (int p = tid; p < P; p += kSelThreads) km = max(km, keys[p]);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) km = max(km, __shfl_xor_sync(0xffffffffu, km, off));
+    if (lane == 0) atomicMax(&s_kmax, km);
+    __syncthreads();
+    const float smax = key_float(s_kmax);
+    const float c2 = a.pol.score_scale * 1.4426950408889634f;
+    u64 tot = 0, man = 0;
+    for (int p = tid; p < P; p += kSelThreads) {
+        const u64 w = page_weight(keys[p], smax, c2);
+        tot += w;
+        if (mand(p)) man += w;
+    }
+    const u64 total = block_sum_u64(tot, red);
+    const u64 held = block_sum_u64(man, red);
+    // weight still to gather from the candidates: ceil(top_p * total) - held
+    const u64 need = (u64)ceil((double)a.pol.top_p * (double)total);
+    if (need <= held) return 0;
+    u64 R = need - held;
+
+    uint32_t prefix = 0, pmask = 0;
+    u64 above = 0;   // weight of the candidates above the current prefix
+    int n_above = 0; // and their count
+    int eq_count = 0;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        hist[tid] = 0;
+        mhist[tid] = 0;
+        __syncthreads();
+        for (int p = tid; p < P; p += kSelThreads) {
+            if (mand(p)) continue;
+            const uint32_t u = keys[p];
+            if ((u & pmask) != prefix) continue;
+            const uint32_t bin = (u >> shift) & 255u;
+            atomicAdd(hist + bin, 1u);
+            atomicAdd(mhist + bin, (u64)page_weight(u, smax, c2));
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // lane l owns bins 255-8l .. 248-8l, visited from the top
+            u64 m[8], msum = 0;
+            int c[8], csum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                m[i] = mhist[255 - 8 * lane - i];
+                c[i] = (int)hist[255 - 8 * lane - i];
+                msum += m[i];
+                csum += c[i];
+            }
+            u64 mincl = msum;
+            int cincl = csum;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const u64 y = __shfl_up_sync(0xffffffffu, mincl, off);
+                const int z = __shfl_up_sync(0xffffffffu, cincl, off);
+                if (lane >= off) {
+                    mincl += y;
+                    cincl += z;
+                }
+            }
+            const u64 mexcl = mincl - msum;
+            const int cexcl = cincl - csum;
+            const unsigned hit = __ballot_sync(0xffffffffu, above + mexcl < R && R <= above + mincl);
+            if (hit == 0) {
+                if (lane == 0) s_digit = -1;  // the candidates cannot reach top_p: take them all
+            } else if (lane == __ffs(hit) - 1) {
+                u64 cm = mexcl;
+                int cc = cexcl;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (above + cm + m[i] >= R) {
+                        s_digit = 255 - 8 * lane - i;
+                        s_mass = cm;   // weight of the higher bins at this level
+                        s_rem = cc;    // and their count
+                        break;
+                    }
+                    cm += m[i];
+                    cc += c[i];
+                }
+            }
+        }
+        __syncthreads();
+        if (s_digit < 0) return ncand;
+        above += s_mass;
+        n_above += s_rem;
+        eq_count = (int)hist[s_digit];
+        prefix |= (uint32_t)s_digit << shift;
+        pmask |= 255u << shift;
+        __syncthreads();  // hist / s_* are rewritten by the next level
+    }
+    // every candidate whose key equals prefix has the same weight
+    const u64 wt = page_weight(prefix, smax, c2);
+    const u64 t = wt ? (R - above + wt - 1) / wt : (u64)eq_count;
+    return n_above + (int)min((u64)eq_count, t);
+}
+
 // Selection of one (sequence, KV head) row by a CTA of 8 warps.  keys holds
 // the row's order-preserving score keys in shared memory.
 __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) {
@@ -79,11 +214,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
     }
     const int sink = min(a.pol.sink_pages, P), local = min(a.pol.local_pages, P);
     const int nm = min(P, sink + local);
-    long long k = budget_pages(a.pol, len, a.ps);
-    if (k > a.k_max) k = a.k_max;
-    if (k < nm) k = nm;
-    if (k > P) k = P;
-    const int kp = (int)k - nm;  // pages to pick among the non-mandatory ones
     const int ncand = P - nm;
     auto mand = [&](int p) { return p < sink || p >= P - local; };
 
@@ -103,6 +233,16 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
         }
     }
     __syncthreads();
+
+    long long k;
+    if (a.pol.mode == SPD_BUDGET_TOP_P)
+        k = nm + top_p_pages(a, keys, P, mand, hist, s_digit, s_rem);
+    else
+        k = budget_pages(a.pol, len, a.ps);
+    if (k > a.k_max) k = a.k_max;
+    if (k < nm) k = nm;
+    if (k > P) k = P;
+    const int kp = (int)k - nm;  // pages to pick among the non-mandatory ones
 
     uint32_t thr;
     int rem;

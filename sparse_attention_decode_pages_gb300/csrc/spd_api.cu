@@ -348,7 +348,10 @@ SPD_API spd_status pages_score_select(const spd_dims* dims, const spd_bf16* q, c
     if (st != SPD_OK) return st;
     if (!policy) return fail(SPD_ERR_INVALID_ARG, "policy is NULL");
     const spd_budget_policy& p = *policy;
-    if (p.mode < 0 || p.mode > 2) return fail(SPD_ERR_INVALID_ARG, "unknown budget mode %d", p.mode);
+    if (p.mode < 0 || p.mode > 3) return fail(SPD_ERR_INVALID_ARG, "unknown budget mode %d", p.mode);
+    if (p.mode == SPD_BUDGET_TOP_P &&
+        (!(p.top_p >= 0.f && p.top_p <= 1.f) || !(p.score_scale > 0.f) || !(p.score_scale < 1e30f)))
+        return fail(SPD_ERR_INVALID_ARG, "top_p must be in [0, 1] and score_scale > 0 and finite");
     if (p.sink_pages < 0 || p.local_pages < 0) return fail(SPD_ERR_INVALID_ARG, "negative sink/local pages");
     if (p.mode == SPD_BUDGET_FIXED_PAGES && p.fixed_pages < 0) return fail(SPD_ERR_INVALID_ARG, "fixed_pages < 0");
     if (p.mode == SPD_BUDGET_LINEAR_TOKENS && (p.slope_den <= 0 || p.slope_num < 0 || p.min_tokens < 0))

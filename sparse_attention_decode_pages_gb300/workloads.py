@@ -82,6 +82,8 @@ class BudgetPolicy:
     mode "linear": ``ceil(max(min_tokens, slope_num * len / slope_den + intercept) / ps)`` pages,
         evaluated in exact integer arithmetic.
     mode "fraction": ``ceil(len * frac_num / (frac_den * ps))`` pages.
+    mode "top_p": the smallest set holding ``top_p`` of the page weight
+        ``exp(score_scale * (score - max score))``, at most k_max pages.
     ``sink_pages`` leading pages and ``local_pages`` trailing pages are always kept.
     """
 
@@ -95,6 +97,8 @@ class BudgetPolicy:
     frac_den: int = 1
     sink_pages: int = 1
     local_pages: int = 1
+    top_p: float = 0.0
+    score_scale: float = 0.0
 
 
 @dataclasses.dataclass

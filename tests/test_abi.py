@@ -57,6 +57,12 @@ def test_validation_rejects_bad_shapes_without_touching_the_gpu(libspd):
     # k_max below sink + local
     assert L.pages_score_select(ctypes.byref(d), None, None, None, ctypes.byref(pol), None,
                                 None, 3, None, None, 0, None) == 1
+    pol_tp = libspd.Policy(3, 0, 0, 1, 0, 0, 1, 1, 1, 1, 1.5, 0.1)  # top_p > 1
+    assert L.pages_score_select(ctypes.byref(d), None, None, None, ctypes.byref(pol_tp), None,
+                                None, 8, None, None, 0, None) == 1
+    pol_tp = libspd.Policy(3, 0, 0, 1, 0, 0, 1, 1, 1, 1, 0.5, 0.0)  # score_scale = 0
+    assert L.pages_score_select(ctypes.byref(d), None, None, None, ctypes.byref(pol_tp), None,
+                                None, 8, None, None, 0, None) == 1
     pol_bad = libspd.Policy(1, 0, 0, 1, 0, 0, 1, 1, 1, 1)  # slope_den = 0
     assert L.pages_score_select(ctypes.byref(d), None, None, None, ctypes.byref(pol_bad),
                                 None, None, 8, None, None, 0, None) == 1

@@ -176,3 +176,79 @@ def test_spec_accept_bad_draft_token_sets_status():
     d["draft"][1, 1] = 512
     na, tk, st = _spec_gpu(d["p"], d["q"], d["draft"], d["u_acc"], d["u_res"])
     assert st == 0x10 and na[1] == 0 and np.all(tk[1] == -1)
+
+
+# ---------------------------------------------------------------- f3 top-p selection
+
+TOP_P_TOL = 1e-3   # relative weight tolerance at the top_p boundary (fp32 scores, 2^-31 grid)
+
+
+def _check_top_p(w, top_p, scale, k_max=None):
+    import dataclasses
+    from tests.gpu_helpers import TIE_BAND
+    k_max = k_max or w.max_pages_per_seq
+    pol = dataclasses.replace(w.policy, mode="top_p", top_p=top_p, score_scale=scale)
+    g = Gpu(w)
+    summ = g.summarize()
+    sel, nsel, sc, _ = g.score_select(summ, policy=pol, k_max=k_max)
+    assert g.sync_status() == 0
+    sel_g, nsel_g, sc_g = sel.cpu().numpy(), nsel.cpu().numpy(), sc.cpu().numpy().astype(np.float64)
+    sc_o = oracle.scores(w, oracle.summarize(w, threads=8), threads=8)
+    sel_o, nsel_o = oracle.select_top_p(w, sc_o, top_p, scale, k_max=k_max, policy=pol)
+    exact = 0
+    for b in range(w.B):
+        P = w.pages(b)
+        sink, local = min(pol.sink_pages, P), min(pol.local_pages, P)
+        mand = {p for p in range(P) if p < sink or p >= P - local}
+        for h in range(w.H_kv):
+            g_set = sel_g[b, h, : nsel_g[b, h]].tolist()
+            o_set = sel_o[b, h, : nsel_o[b, h]].tolist()
+            assert g_set == sorted(set(g_set)) and mand <= set(g_set)
+            if g_set == o_set:
+                exact += 1
+                continue
+            s = sc_o[b, h, :P]
+            wgt = np.exp(scale * (s - s.max()))
+            need = top_p * wgt.sum()
+            order = sorted((p for p in range(P) if p not in mand), key=lambda p: (-s[p], p))
+            n = len(g_set) - len(mand)
+            held = lambda m: wgt[list(mand)].sum() + wgt[order[:m]].sum()
+            # the count is right up to the weight tolerance
+            assert n == k_max - len(mand) or held(n) >= need * (1 - TOP_P_TOL), (b, h, n)
+            assert n == 0 or held(n - 1) < need * (1 + TOP_P_TOL), (b, h, n)
+            # the pages are the best n by score, up to the tie band
+            kth = s[order[n - 1]] if n else np.inf
+            band = {p for p in order if abs(s[p] - kth) <= TIE_BAND * abs(kth)}
+            assert set(g_set) - band == (set(order[:n]) | mand) - band, (b, h)
+    return exact
+
+
+@pytest.mark.parametrize("top_p", [0.0, 0.5, 0.9, 0.99, 1.0])
+def test_top_p_selection_matches_oracle(top_p):
+    w = wl.named("q8b", threads=4, B=5, len_lo=700, len_hi=2200)
+    exact = _check_top_p(w, top_p, 1.0 / np.sqrt(w.D))
+    assert exact >= w.B * w.H_kv // 2
+
+
+@pytest.mark.parametrize("name,kw,scale", [
+    ("sweep", dict(page_size=32, B=3, len_lo=2000, len_hi=6000), 0.05),
+    ("longtail", dict(B=2, len_lo=4000, len_hi=9000, T=1), 0.2),
+    ("tiny", dict(), 0.125)])
+def test_top_p_selection_other_workloads(name, kw, scale):
+    w = wl.named(name, threads=4, **kw)
+    _check_top_p(w, 0.8, scale)
+    _check_top_p(w, 0.8, scale, k_max=max(8, w.policy.sink_pages + w.policy.local_pages))
+
+
+def test_top_p_then_sparse_attention():
+    """The top-p selection feeds the sparse attention like a top-k one."""
+    import dataclasses
+    from tests.gpu_helpers import assert_close_outputs, np_bf16
+    w = wl.named("q8b", threads=4, B=3, len_lo=800, len_hi=1500)
+    pol = dataclasses.replace(w.policy, mode="top_p", top_p=0.7, score_scale=1.0 / np.sqrt(w.D))
+    g = Gpu(w)
+    sel, nsel, _, _ = g.score_select(g.summarize(), policy=pol, k_max=w.max_pages_per_seq)
+    o, lse, _ = g.sparse_attn(sel, nsel)
+    assert g.sync_status() == 0
+    o_ref, lse_ref = oracle.sparse_attn(w, sel.cpu().numpy(), nsel.cpu().numpy(), threads=8)
+    assert_close_outputs(np_bf16(o), o_ref, lse.cpu().numpy(), lse_ref)
