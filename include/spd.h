@@ -328,6 +328,73 @@ spd_status spec_accept(int32_t B, int32_t k, int32_t n_vocab, const float *p_dra
 spd_status lse_merge(int32_t S, int32_t rows, int32_t D, const float *part_o,
                      const float *part_lse, spd_bf16 *o, float *lse, void *stream);
 
+/*
+ * spd_round -- one S3R round captured as CUDA graphs: k sparse draft steps,
+ * then dense verification of the k + 1 positions and exact speculative
+ * sampling, replayed with one graph launch per part (S3R Table 7: drafting
+ * runs under CUDA Graphs; "Draft (6Tq)" and "Verify (TV)" are its two parts).
+ *
+ * Draft step s (0 <= s < k), on lengths seq_lens[s][:] (which count the token
+ * the step appends):
+ *   kv_append_refresh(T = 1, k_draft[s], v_draft[s]);
+ *   pages_score_select(q_draft[s]) into sel / nsel (reused by every step);
+ *   sparse_decode_attn(q_draft[s]) -> o_draft[s], lse_draft[s].
+ * Verification, on lengths seq_lens[k][:]:
+ *   kv_append_refresh(T = k + 1, k_verify, v_verify)   (rewrites the positions);
+ *   dense_verify_attn(T = k + 1, q_verify) -> o_verify, lse_verify;
+ *   spec_accept(...) -> n_accepted, tokens            (skipped when n_vocab = 0).
+ * Layouts: seq_lens int32 [k + 1][B]; q_draft bf16 [k][B][H_q][D]; k_draft,
+ * v_draft bf16 [k][B][H_kv][D]; q_verify bf16 [B][k+1][H_q][D]; k_verify,
+ * v_verify bf16 [B][k+1][H_kv][D]; o_draft [k][B][H_q][D]; lse_draft
+ * [k][B][H_q] (may be NULL); o_verify / lse_verify as dense_verify_attn; the
+ * sampling buffers as spec_accept.  The three workspaces are sized by the
+ * matching *_workspace_size calls; the split counts and softmax_scale mean
+ * what they mean in those calls.
+ *
+ * spd_round_create validates the descriptor, makes each call once on a
+ * private stream under capture (so every argument error surfaces here, with
+ * nothing launched) and instantiates the graphs; the buffers must stay valid
+ * and keep their addresses for the life of the round.  spd_round_launch
+ * replays part 0 (draft steps), 1 (verification) or 2 (both, in order) on
+ * `stream`; replaying is the same computation as making the calls.  Make one
+ * ordinary call of the library on the device before the first create.
+ */
+typedef struct {
+    spd_dims dims;
+    int32_t k; /* draft steps per round, 1 <= k <= 32 */
+    spd_bf16 *K, *V, *summ;
+    const int32_t *page_table;
+    const int32_t *seq_lens;
+    const spd_bf16 *q_draft, *k_draft, *v_draft;
+    const spd_bf16 *q_verify, *k_verify, *v_verify;
+    spd_budget_policy policy;
+    int32_t k_max;
+    int32_t *sel, *nsel;
+    spd_bf16 *o_draft;
+    float *lse_draft;
+    spd_bf16 *o_verify;
+    float *lse_verify;
+    int32_t n_vocab;
+    const float *p_draft, *q_target;
+    const int32_t *draft_tokens;
+    const float *u_acc, *u_res;
+    int32_t *n_accepted, *tokens;
+    void *ws_select;
+    size_t ws_select_bytes;
+    void *ws_sparse;
+    size_t ws_sparse_bytes;
+    void *ws_verify;
+    size_t ws_verify_bytes;
+    int32_t sparse_splits, verify_splits;
+    float softmax_scale;
+} spd_round_desc;
+
+typedef struct spd_round_s spd_round;
+
+spd_status spd_round_create(const spd_round_desc *desc, spd_round **out);
+spd_status spd_round_launch(spd_round *round, int32_t part, void *stream);
+void spd_round_destroy(spd_round *round);
+
 #ifdef __cplusplus
 }
 #endif

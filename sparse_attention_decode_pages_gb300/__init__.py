@@ -54,6 +54,27 @@ class Policy(ctypes.Structure):
                 ("top_p", ctypes.c_float), ("score_scale", ctypes.c_float)]
 
 
+class RoundDesc(ctypes.Structure):
+    _fields_ = [("dims", Dims), ("k", ctypes.c_int32),
+                ("K", ctypes.c_void_p), ("V", ctypes.c_void_p), ("summ", ctypes.c_void_p),
+                ("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("q_draft", ctypes.c_void_p), ("k_draft", ctypes.c_void_p), ("v_draft", ctypes.c_void_p),
+                ("q_verify", ctypes.c_void_p), ("k_verify", ctypes.c_void_p), ("v_verify", ctypes.c_void_p),
+                ("policy", Policy), ("k_max", ctypes.c_int32),
+                ("sel", ctypes.c_void_p), ("nsel", ctypes.c_void_p),
+                ("o_draft", ctypes.c_void_p), ("lse_draft", ctypes.c_void_p),
+                ("o_verify", ctypes.c_void_p), ("lse_verify", ctypes.c_void_p),
+                ("n_vocab", ctypes.c_int32),
+                ("p_draft", ctypes.c_void_p), ("q_target", ctypes.c_void_p),
+                ("draft_tokens", ctypes.c_void_p), ("u_acc", ctypes.c_void_p), ("u_res", ctypes.c_void_p),
+                ("n_accepted", ctypes.c_void_p), ("tokens", ctypes.c_void_p),
+                ("ws_select", ctypes.c_void_p), ("ws_select_bytes", ctypes.c_size_t),
+                ("ws_sparse", ctypes.c_void_p), ("ws_sparse_bytes", ctypes.c_size_t),
+                ("ws_verify", ctypes.c_void_p), ("ws_verify_bytes", ctypes.c_size_t),
+                ("sparse_splits", ctypes.c_int32), ("verify_splits", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float)]
+
+
 _lib = None
 
 
@@ -86,9 +107,14 @@ def lib():
         L.lse_merge.argtypes = [i32, i32, i32, P, P, P, P, P]
         L.kv_append_refresh.argtypes = [DP, i32, P, P, P, P, P, P, P, P]
         L.spec_accept.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, P]
+        L.spd_round_create.argtypes = [ctypes.POINTER(RoundDesc), ctypes.POINTER(ctypes.c_void_p)]
+        L.spd_round_launch.argtypes = [P, i32, P]
+        L.spd_round_destroy.argtypes = [P]
+        L.spd_round_destroy.restype = None
         for f in ("spd_device_status", "pages_summarize", "pages_score_select",
                   "sparse_decode_attn", "dense_verify_attn", "lse_merge",
-                  "sparse_decode_attn_noalloc", "kv_append_refresh", "spec_accept"):
+                  "sparse_decode_attn_noalloc", "kv_append_refresh", "spec_accept",
+                  "spd_round_create", "spd_round_launch"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -220,3 +246,50 @@ def lse_merge(part_o, part_lse, o, lse=None, stream=None):
     S, rows, D = part_o.shape
     _check(lib().lse_merge(S, rows, D, _ptr(part_o), _ptr(part_lse), _ptr(o), _ptr(lse),
                            _stream(stream)))
+
+
+class Round:
+    """spd_round: one S3R round (k sparse draft steps, verification, sampling) as two
+    CUDA graphs built by the library.  Takes device tensors laid out as include/spd.h
+    states; keeps them referenced while the round lives.  ``sampling`` is None or a dict
+    with p_draft, q_target, draft_tokens, u_acc, u_res, n_accepted, tokens."""
+
+    def __init__(self, dims: Dims, k: int, K, V, summ, page_table, seq_lens, q_draft, k_draft,
+                 v_draft, q_verify, k_verify, v_verify, policy, k_max: int, sel, nsel, o_draft,
+                 o_verify, ws_select, ws_sparse, ws_verify, lse_draft=None, lse_verify=None,
+                 sampling=None, sparse_splits: int = 0, verify_splits: int = 0,
+                 softmax_scale: float | None = None):
+        pol = policy if isinstance(policy, Policy) else policy_of(policy)
+        scale = 1.0 / math.sqrt(dims.D) if softmax_scale is None else softmax_scale
+        smp = sampling or {}
+        self._keep = [K, V, summ, page_table, seq_lens, q_draft, k_draft, v_draft, q_verify,
+                      k_verify, v_verify, sel, nsel, o_draft, o_verify, ws_select, ws_sparse,
+                      ws_verify, lse_draft, lse_verify, *smp.values()]
+        n_vocab = int(smp["q_target"].shape[-1]) if smp else 0
+        g = lambda name: _ptr(smp.get(name))
+        d = RoundDesc(dims, k, _ptr(K), _ptr(V), _ptr(summ), _ptr(page_table), _ptr(seq_lens),
+                      _ptr(q_draft), _ptr(k_draft), _ptr(v_draft), _ptr(q_verify), _ptr(k_verify),
+                      _ptr(v_verify), pol, k_max, _ptr(sel), _ptr(nsel), _ptr(o_draft),
+                      _ptr(lse_draft), _ptr(o_verify), _ptr(lse_verify), n_vocab,
+                      g("p_draft"), g("q_target"), g("draft_tokens"), g("u_acc"), g("u_res"),
+                      g("n_accepted"), g("tokens"),
+                      _ptr(ws_select), ws_select.numel(), _ptr(ws_sparse), ws_sparse.numel(),
+                      _ptr(ws_verify), ws_verify.numel(), sparse_splits, verify_splits, scale)
+        h = ctypes.c_void_p()
+        _check(lib().spd_round_create(ctypes.byref(d), ctypes.byref(h)))
+        self._h = h
+
+    def launch(self, part: int = 2, stream=None):
+        """Replay part 0 (draft steps), 1 (verification + sampling) or 2 (both)."""
+        _check(lib().spd_round_launch(self._h, part, _stream(stream)))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().spd_round_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

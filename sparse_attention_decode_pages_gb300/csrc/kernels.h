@@ -102,6 +102,10 @@ cudaError_t launch_dense_attn(const AttnArgs& a, const CUtensorMap& tmK, const C
 int occ_sparse_attn(int D, int ps);
 int occ_dense_attn(int D, int ps, int mtiles);
 
+// Host helpers of the C-ABI layer shared with round.cu.
+spd_status device_ready();
+spd_status set_error(spd_status s, const char* msg);
+
 cudaError_t launch_lse_merge(int S, int rows, int D, const float* part_o, const float* part_lse,
                              uint16_t* o, float* lse, cudaStream_t st);
 

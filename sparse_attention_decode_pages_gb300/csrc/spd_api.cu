@@ -107,6 +107,18 @@ spd_status kv_map(CUtensorMap* m, const void* base, const spd_dims* d) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+// Per-device set-up of the current device (status word, SM count), done once.
+spd_status device_ready() {
+    spd_status st = SPD_OK;
+    return dev_info(&st) ? SPD_OK : st;
+}
+
+spd_status set_error(spd_status s, const char* msg) { return fail(s, "%s", msg); }
+
+namespace {
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 spd_status check_dims(const spd_dims* d) {

@@ -356,3 +356,27 @@ def spec_inputs(B: int = 64, k: int = 6, n: int = VOCAB_QWEN3, seed: int = 1006,
     u_acc = rng.random((B, k), dtype=np.float32)
     u_res = rng.random(B, dtype=np.float32)
     return dict(p=p, q=q, draft=draft, u_acc=u_acc, u_res=u_res)
+
+
+def round_inputs(w: Workload, k: int = 6, seed: int = 1007, n_vocab: int = 0) -> dict:
+    """Seeded inputs of one S3R round on workload ``w`` (k sparse draft steps, then
+    verification of k + 1 positions), with w.seq_lens as the verification lengths.
+
+    Draft step s appends position L0 + s with L0 = seq_lens - (k + 1), so its lengths
+    are L0 + s + 1.  Returns seq_lens int32 [k+1][B]; q_draft [k][B][H_q][D],
+    k_draft / v_draft [k][B][H_kv][D], q_verify [B][k+1][H_q][D], k_verify / v_verify
+    [B][k+1][H_kv][D] (bf16 bits, N(0, 1)); with n_vocab > 0 also the sampling inputs
+    of ``spec_inputs`` (p, q, draft, u_acc, u_res)."""
+    rng = np.random.default_rng(seed)
+    B, Hq, Hkv, D = w.B, w.H_q, w.H_kv, w.D
+    L0 = w.seq_lens.astype(np.int64) - (k + 1)
+    if L0.min() < 0:
+        raise ValueError("every sequence needs at least k + 1 tokens")
+    lens = np.stack([L0 + s + 1 for s in range(k)] + [w.seq_lens.astype(np.int64)]).astype(np.int32)
+    bf = lambda shape: f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32))
+    out = dict(seq_lens=lens, q_draft=bf((k, B, Hq, D)), k_draft=bf((k, B, Hkv, D)),
+               v_draft=bf((k, B, Hkv, D)), q_verify=bf((B, k + 1, Hq, D)),
+               k_verify=bf((B, k + 1, Hkv, D)), v_verify=bf((B, k + 1, Hkv, D)))
+    if n_vocab:
+        out.update(spec_inputs(B=B, k=k, n=n_vocab, seed=seed + 1))
+    return out
