@@ -314,6 +314,9 @@ def run_gpu(args):
     h2d = q_h.numel() * 2 + sl_h.numel() * 4 + pt_h.numel() * 4 + (kn_h.numel() + vn_h.numel()) * 2
     d2h = o_h.numel() * 2 + lse_h.numel() * 4
 
+    nxt = None if args.no_next else next_rows(spd, torch, w, d, dims, summ, stream, flush, peak_of=hbm_peak,
+                                              reps=max(10, min(args.steps, 50)), warmup=args.warmup)
+
     # max over ranks
     vals = torch.tensor([ms_step, ms_ver, float(np.mean(e2e_ms)), ms_att], device=dev, dtype=torch.float64)
     if world > 1:
@@ -383,10 +386,114 @@ def run_gpu(args):
             "clocks": clocks,
             "wall_s_timed_region": t1 - t0,
             "cpu_baseline": cpu,
+            "next_rows": nxt,
         }
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def _timed(torch, stream, flush, fn, reps, warmup):
+    """Median device time (ms) of fn() between events on the stream, L2 evicted before each."""
+    for _ in range(warmup):
+        fn()
+    out = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        out.append(a.elapsed_time(b))
+    return float(np.median(out))
+
+
+def next_rows(spd, torch, w, d, dims, summ, stream, flush, peak_of, reps, warmup):
+    """The rows after the core path, measured on the same workload after its timed region:
+    exact speculative sampling (B sequences, k = 6, Qwen3's vocabulary), top-p page
+    selection, and the S3R round as CUDA graphs against the same calls made eagerly."""
+    import dataclasses
+    dev = d["q"].device
+    peak, _ = peak_of()
+    k = 6
+    res = {}
+    # f2: speculative sampling
+    sp = wl.spec_inputs(B=w.B, k=k)
+    P = torch.from_numpy(sp["p"]).to(dev)
+    Q = torch.from_numpy(sp["q"]).to(dev)
+    Dr = torch.from_numpy(sp["draft"]).to(dev)
+    Ua = torch.from_numpy(sp["u_acc"]).to(dev)
+    Ur = torch.from_numpy(sp["u_res"]).to(dev)
+    na = torch.empty(w.B, dtype=torch.int32, device=dev)
+    tk = torch.empty((w.B, k + 1), dtype=torch.int32, device=dev)
+    ms = _timed(torch, stream, flush, lambda: spd.spec_accept(P, Q, Dr, Ua, Ur, na, tk), reps, warmup)
+    nacc = na.cpu().numpy()
+    n = sp["p"].shape[-1]
+    rows = sum(2 if a < k else 1 for a in nacc)   # residual rows read p and q; the bonus row q only
+    byts = rows * n * 4 + w.B * k * 16
+    res["f2_spec_accept"] = {"us": ms * 1e3, "bytes": byts, "achieved_gbs": byts / (ms * 1e-3) / 1e9,
+                             "frac": byts / (ms * 1e-3) / 1e9 / peak, "k": k, "n_vocab": n,
+                             "mean_accepted": float(nacc.mean())}
+    del P, Q
+    # f3: top-p selection (scores + select) against the fixed top-k budget
+    pol = dataclasses.replace(w.policy, mode="top_p", top_p=0.9, score_scale=1.0 / math.sqrt(w.D))
+    k_max = w.max_pages_per_seq
+    sel = torch.empty((w.B, w.H_kv, k_max), dtype=torch.int32, device=dev)
+    nsel = torch.empty((w.B, w.H_kv), dtype=torch.int32, device=dev)
+    ws = spd.workspace(spd.spd_score_select_workspace_size(dims), dev)
+    ms = _timed(torch, stream, flush, lambda: spd.pages_score_select(dims, d["q"], summ, d["seq_lens"], pol, sel,
+                                                                     nsel, k_max, ws), reps, warmup)
+    res["f3_top_p_score_select"] = {"us": ms * 1e3, "top_p": 0.9, "mean_pages": float(nsel.float().mean()),
+                                    "max_pages": int(nsel.max())}
+    # f4: one S3R round (6 draft steps; verification of 7 positions + sampling) as graphs vs eager
+    r = wl.round_inputs(w, k=k, n_vocab=n)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).to(dev)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+    lens = i32(r["seq_lens"])
+    qd, kd, vd = bf(r["q_draft"]), bf(r["k_draft"]), bf(r["v_draft"])
+    qv, kv, vv = bf(r["q_verify"]), bf(r["k_verify"]), bf(r["v_verify"])
+    smp = dict(p_draft=f32(r["p"]), q_target=f32(r["q"]), draft_tokens=i32(r["draft"]), u_acc=f32(r["u_acc"]),
+               u_res=f32(r["u_res"]), n_accepted=torch.zeros(w.B, dtype=torch.int32, device=dev),
+               tokens=torch.zeros((w.B, k + 1), dtype=torch.int32, device=dev))
+    kx = w.k_max
+    sel = torch.empty((w.B, w.H_kv, kx), dtype=torch.int32, device=dev)
+    nsel = torch.empty((w.B, w.H_kv), dtype=torch.int32, device=dev)
+    od = torch.empty((k, w.B, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
+    ov = torch.empty((w.B, k + 1, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
+    ws_sel = spd.workspace(spd.spd_score_select_workspace_size(dims), dev)
+    ws_sp = spd.workspace(spd.spd_sparse_decode_workspace_size(dims, kx, 0), dev)
+    ws_ver = spd.workspace(spd.spd_dense_verify_workspace_size(dims, k + 1, 0), dev)
+    K, V, pt = d["K"], d["V"], d["page_table"]
+
+    def eager_draft():
+        for s_ in range(k):
+            spd.kv_append_refresh(dims, 1, K, V, pt, lens[s_], kd[s_], vd[s_], summ)
+            spd.pages_score_select(dims, qd[s_], summ, lens[s_], w.policy, sel, nsel, kx, ws_sel)
+            spd.sparse_decode_attn(dims, qd[s_], K, V, pt, lens[s_], sel, nsel, kx, od[s_], ws_sp)
+
+    def eager_verify():
+        spd.kv_append_refresh(dims, k + 1, K, V, pt, lens[k], kv, vv, summ)
+        spd.dense_verify_attn(dims, k + 1, qv, K, V, pt, lens[k], ov, ws_ver)
+        spd.spec_accept(smp["p_draft"], smp["q_target"], smp["draft_tokens"], smp["u_acc"], smp["u_res"],
+                        smp["n_accepted"], smp["tokens"])
+
+    rnd = spd.Round(dims, k, K, V, summ, pt, lens, qd, kd, vd, qv, kv, vv, w.policy, kx, sel, nsel, od, ov,
+                    ws_sel, ws_sp, ws_ver, sampling=smp)
+    e_d = _timed(torch, stream, flush, eager_draft, reps, warmup)
+    e_v = _timed(torch, stream, flush, eager_verify, reps, warmup)
+    g_d = _timed(torch, stream, flush, lambda: rnd.launch(0, stream), reps, warmup)
+    g_v = _timed(torch, stream, flush, lambda: rnd.launch(1, stream), reps, warmup)
+    acc = smp["n_accepted"].float().mean().item()
+    rnd.close()
+    res["f4_s3r_round"] = {"k": k, "draft_graph_ms": g_d, "verify_graph_ms": g_v, "draft_eager_ms": e_d,
+                           "verify_eager_ms": e_v, "mean_accepted": acc,
+                           "round_tokens_per_s": w.B * (acc + 1) / ((g_d + g_v) * 1e-3),
+                           "note": "L2 evicted before each part; the 6 draft steps run back to back inside it"}
+    if spd.spd_device_status(clear=True):
+        raise RuntimeError("device status set while measuring the next rows")
+    return res
 
 
 def _oracle_sparse_step(w, summ, threads):
@@ -458,6 +565,7 @@ def main():
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--vsplits", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next", action="store_true", help="skip the measurements of the rows after the core path")
     ap.add_argument("--batch", type=int, default=0, help="override B (small profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
