@@ -48,7 +48,7 @@ METRIC = "sparse decode-attn tokens/s and HBM GB/s (% of roofline), Qwen3-8B sha
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20  # read between timed passes: evicts L2 (129 MB) and leaves it clean
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = ["common.cuh", "attn.cuh", "attn_sparse.cu", "score_select.cu", "summarize.cu"]
+KERNEL_SOURCES = ["common.cuh", "kernels.h", "attn.cuh", "attn_sparse.cu"]  # the sparse attention kernel
 
 
 def kernel_source_hash() -> str:
