@@ -47,37 +47,46 @@ struct UnitInfo {
     int nsplit;  // units of this row
 };
 
-template <int D, int PS, int NMT, bool SPARSE>
+template <int D, int PS, int NMT, bool SPARSE, int KS>
 struct AttnCfg {
     static constexpr int TILE = PS * D * 2;  // bytes of one K (or V) tile
     static constexpr int SLOT = 2 * TILE;
-    // ring depth: ~32-64 KB of K/V in flight per worker
-    static constexpr int STAGES = SLOT <= 8192 ? 4 : (SLOT <= 16384 ? 3 : 2);
-    static constexpr int THREADS = (NMT + 1) * 32;  // consumers + one producer warp
-    static constexpr int RP = NMT * 16;             // padded rows
+    // ring depth: ~32-64 KB of K/V in flight per worker, a multiple of KS
+    static constexpr int STAGES = KS == 1 ? (SLOT <= 8192 ? 4 : (SLOT <= 16384 ? 3 : 2))
+                                          : (SLOT <= 16384 ? 2 * KS : KS);
+    static constexpr int CONSUMERS = NMT * KS;            // KS groups of NMT warps
+    static constexpr int THREADS = (CONSUMERS + 1) * 32;  // consumers + one producer warp
+    static constexpr int RP = NMT * 16;                   // padded rows
     // A Q buffer holds the unit's R real rows (decode: R = G <= 8; verify:
     // R <= RP); padding rows are zero in registers.
     static constexpr int QROWS = SPARSE ? 8 : RP;
     static constexpr int QBYTES = QROWS * D * 2;
-    static constexpr int NQ = STAGES + 1;           // Q buffers: at most STAGES + 1 units are live
-    static constexpr int FIFO = 8;                  // unit-info entries (>= STAGES + 1)
+    // Q buffers per group: every unit spans >= KS items (it is padded to a
+    // multiple of KS), so at most STAGES / KS + 1 units have items in the ring.
+    static constexpr int NQ = STAGES / KS + 1;
+    static constexpr int FIFO = 8;  // unit-info entries (>= NQ)
+    // Per consumer lane of groups 1..KS-1: its O fragments, then m0, m1, l0, l1.
+    static constexpr int MERGE_FLOATS = 4 * (D / 8) + 4;
+    static constexpr int MERGE = KS > 1 ? (KS - 1) * NMT * 32 * MERGE_FLOATS * 4 : 0;
     static constexpr int OFF_Q = STAGES * SLOT;
-    static constexpr int OFF_BAR = OFF_Q + NQ * QBYTES;          // full[STAGES], empty[STAGES]
-    static constexpr int OFF_FIFO = OFF_BAR + 2 * STAGES * 8;
+    static constexpr int OFF_MERGE = OFF_Q + NQ * KS * QBYTES;
+    static constexpr int OFF_BAR = OFF_MERGE + MERGE;  // full[STAGES], empty[STAGES], merge_full, merge_empty
+    static constexpr int OFF_FIFO = OFF_BAR + (2 * STAGES + 2) * 8;
     static constexpr int OFF_META = OFF_FIFO + FIFO * (int)sizeof(UnitInfo);  // int2 per slot
     static constexpr int BODY = OFF_META + STAGES * 8;
     static constexpr int SMEM = 1024 /*alignment slack*/ + BODY;
-    static_assert(STAGES + 1 <= NQ && STAGES + 1 <= FIFO, "ring deeper than the unit buffers");
+    static_assert(STAGES % KS == 0, "each ring slot must belong to one consumer group");
+    static_assert(NQ <= FIFO, "ring deeper than the unit buffers");
 };
 
 constexpr int kEndOfWork = -2;  // slot_meta.x: no more items
 constexpr float kRescale = 8.f;  // log2 headroom before the running max moves
 
-template <int D, int PS, int NMT, bool SPARSE>
-__global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
+template <int D, int PS, int NMT, bool SPARSE, int KS>
+__global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV) {
-    using C = AttnCfg<D, PS, NMT, SPARSE>;
+    using C = AttnCfg<D, PS, NMT, SPARSE, KS>;
     constexpr int STAGES = C::STAGES;
     constexpr int KSTEPS = D / 16;
     constexpr int NT_O = D / 8;
@@ -91,6 +100,8 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
     uint8_t* qbuf = smem + C::OFF_Q;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* empty = full + STAGES;
+    uint64_t* merge_full = empty + STAGES;  // groups 1..KS-1 have written their state
+    uint64_t* merge_empty = merge_full + 1; // group 0 has read it
     UnitInfo* fifo = reinterpret_cast<UnitInfo*>(smem + C::OFF_FIFO);
     int2* slot_meta = reinterpret_cast<int2*>(smem + C::OFF_META);  // {logical page or -1 / end, unit seq}
 
@@ -104,6 +115,10 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
             mbar_init(full + i, 1);
             mbar_init(empty + i, NMT);
         }
+        if (KS > 1) {
+            mbar_init(merge_full, (KS - 1) * NMT);
+            mbar_init(merge_empty, NMT);
+        }
         mbar_fence_init();
     }
     __syncthreads();
@@ -115,7 +130,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
         return ((long long)b * a.T + t) * a.H_q + h * G + g;
     };
 
-    if (warp == NMT) {
+    if (warp == C::CONSUMERS) {
         // ============================================================ producer warp
         if (lane == 0) {
             tma_prefetch_desc(&tmK);
@@ -133,13 +148,24 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
                 r = mbar_wait_bounded(empty + (jj % STAGES), (uint32_t)(((jj / STAGES) - 1) & 1), a.status);
             return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
         };
+        bool first_unit = true;
         while (ok) {
-            unsigned long long u = 0;
-            if (lane == 0) u = atomicAdd(reinterpret_cast<unsigned long long*>(queue), 1ull);
-            u = __shfl_sync(0xffffffffu, u, 0);
+            // The first unit of CTA i is unit i (the grid never exceeds the units);
+            // later ones come from the queue, which counts past the grid.
+            unsigned long long u = blockIdx.x;
+            if (!first_unit) {
+                if (lane == 0) u = gridDim.x + atomicAdd(reinterpret_cast<unsigned long long*>(queue), 1ull);
+                u = __shfl_sync(0xffffffffu, u, 0);
+            }
+            first_unit = false;
             if ((long long)u >= total_units) break;
             const int row = (int)(u / a.num_splits), split = (int)(u % a.num_splits);
             const int b = row / a.H_kv, h = row - b * a.H_kv;
+            const int start = split * a.items_per_split;
+            // The first 32 selection entries are loaded together with the length
+            // and the count (one round trip instead of two).
+            int pre = -1;
+            if (SPARSE && start + lane < a.k_max) pre = a.sel[(long long)row * a.k_max + start + lane];
             const int len = a.seq_lens[b];
             const int P = (len + PS - 1) / PS;
             int n_items;
@@ -152,7 +178,6 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
             } else {
                 n_items = P;
             }
-            const int start = split * a.items_per_split;
             const int count = min(a.items_per_split, n_items - start);
             if (count <= 0) {
                 if (split == 0)  // empty row: o = 0, lse = -inf
@@ -174,13 +199,16 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
                 info.nsplit = (n_items + a.items_per_split - 1) / a.items_per_split;
                 fifo[seq % C::FIFO] = info;  // published by the first item's arrive (release)
             }
-            for (int base = 0; base < count && ok; base += 32) {
+            // Items are issued in multiples of KS (padding items carry no page), so
+            // every unit starts on group 0 and each group sees each unit.
+            const int cpad = (count + KS - 1) / KS * KS;
+            for (int base = 0; base < cpad && ok; base += 32) {
                 // resolve 32 items in one round trip
                 int lp = -1;
                 long long phys = -1;
                 if (base + lane < count) {
                     const int it = start + base + lane;
-                    lp = SPARSE ? a.sel[(long long)row * a.k_max + it] : it;
+                    lp = SPARSE ? (base == 0 ? pre : a.sel[(long long)row * a.k_max + it]) : it;
                     if (lp < 0 || lp >= P) {
                         raise_status(a.status, SPD_DEV_BAD_SEL);
                         lp = -1;
@@ -192,7 +220,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
                         }
                     }
                 }
-                const int nb = min(32, count - base);
+                const int nb = min(32, cpad - base);
                 for (int k = 0; k < nb; ++k) {
                     const int lpk = __shfl_sync(0xffffffffu, lp, k);
                     const long long pk = __shfl_sync(0xffffffffu, phys, k);
@@ -203,12 +231,13 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
                     if (lane == 0) {
                         const int slot = (int)(j % STAGES);
                         slot_meta[slot] = make_int2(lpk, seq);
-                        const bool first = (base + k == 0);
+                        // each group's first item of the unit carries that group's copy of Q
+                        const bool first = (base + k < KS);
                         uint32_t bytes = lpk >= 0 ? (uint32_t)C::SLOT : 0u;
                         if (first) bytes += (uint32_t)(R * D * 2);
                         mbar_arrive_expect_tx(full + slot, bytes);
                         if (first) {  // the unit's Q rows: T runs of G*D contiguous bf16
-                            uint8_t* qd = qbuf + (seq % C::NQ) * C::QBYTES;
+                            uint8_t* qd = qbuf + ((seq % C::NQ) * KS + (base + k)) * C::QBYTES;
                             const bf16* qs = reinterpret_cast<const bf16*>(a.q);
                             for (int t = 0; t < a.T; ++t)
                                 bulk_load(qd + t * G * D * 2, qs + (((long long)b * a.T + t) * a.H_q + h * G) * D,
@@ -229,11 +258,15 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
             }
             ++seq;
         }
-        // End of work, signalled through the ring.
-        if (ok && slot_free(j) && lane == 0) {
-            const int slot = (int)(j % STAGES);
-            slot_meta[slot] = make_int2(kEndOfWork, seq);
-            mbar_arrive_expect_tx(full + slot, 0);
+        // End of work, signalled through the ring (once per consumer group).
+        for (int e = 0; e < KS && ok; ++e) {
+            if (!slot_free(j)) break;
+            if (lane == 0) {
+                const int slot = (int)(j % STAGES);
+                slot_meta[slot] = make_int2(kEndOfWork, seq);
+                mbar_arrive_expect_tx(full + slot, 0);
+            }
+            ++j;
         }
         // The last producer to finish resets the queue for the next call.
         if (lane == 0) {
@@ -249,7 +282,11 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
     }
 
     // ============================================================ consumer warps
-    const int mt = warp;
+    // Group kg takes the items j = kg (mod KS) of every unit (page-parallel), warp
+    // mt of the group the 16-row tile mt.  Groups 1..KS-1 hand their softmax
+    // state to group 0 at the end of each unit, which finishes the unit.
+    const int kg = warp / NMT;
+    const int mt = warp - kg * NMT;
     const int qr0 = mt * 16 + (lane >> 2), qr1 = qr0 + 8;
     const int c4 = lane & 3;
     uint32_t qa[KSTEPS][4];
@@ -258,7 +295,8 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
     int lim0 = 0, lim1 = 0, lim_min = 0;
     UnitInfo cu;
     cu.count = 0;
-    int cur_seq = -1, c_item = 0;
+    int cur_seq = -1, c_item = 0, g_items = 0;
+    unsigned units_done = 0;  // units this warp has finished (merge barrier phases)
     // consumer-only barrier (the producer warp never joins it)
     auto consumers_sync = [&]() {
         if (NMT > 1)
@@ -267,7 +305,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
             __syncwarp();
     };
 
-    for (long long j = 0;; ++j) {
+    for (long long j = kg;; j += KS) {
         const int slot = (int)(j % STAGES);
         if (!mbar_wait_bounded(full + slot, (uint32_t)((j / STAGES) & 1), a.status)) break;
         const int2 meta = slot_meta[slot];
@@ -277,7 +315,8 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
             cur_seq = meta.y;
             cu = fifo[cur_seq % C::FIFO];
             c_item = 0;
-            const uint8_t* qsm = qbuf + (cur_seq % C::NQ) * C::QBYTES;
+            g_items = (cu.count + KS - 1) / KS;
+            const uint8_t* qsm = qbuf + ((cur_seq % C::NQ) * KS + kg) * C::QBYTES;
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
                 const int d0 = kk * 16 + 2 * c4;
@@ -409,9 +448,54 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
         // This warp is done with the slot.
         __syncwarp();
         if (lane == 0) mbar_arrive(empty + slot);
-        if (++c_item < cu.count) continue;
+        if (++c_item < g_items) continue;
 
         // ---------------------------------------------------------- unit epilogue
+        if constexpr (KS > 1) {
+            // Groups 1..KS-1 dump their state (same fragment layout lane for lane);
+            // group 0 rescales everything to a common base and adds it up.  The
+            // hand-over uses two mbarriers, so every wait in it is bounded.
+            float* mb = reinterpret_cast<float*>(smem + C::OFF_MERGE);
+            const uint32_t ph = units_done & 1u;
+            ++units_done;
+            if (kg > 0) {
+                // the previous unit's state must have been read before it is overwritten
+                if (units_done > 1 && !mbar_wait_bounded(merge_empty, ph ^ 1u, a.status)) break;
+                float* dst = mb + ((long long)((kg - 1) * NMT + mt) * 32 + lane) * C::MERGE_FLOATS;
+#pragma unroll
+                for (int i = 0; i < NT_O; ++i)
+                    *reinterpret_cast<float4*>(dst + 4 * i) = make_float4(oacc[i][0], oacc[i][1], oacc[i][2], oacc[i][3]);
+                *reinterpret_cast<float4*>(dst + 4 * NT_O) = make_float4(m0, m1, l0, l1);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(merge_full);
+                continue;
+            }
+            if (!mbar_wait_bounded(merge_full, ph, a.status)) break;
+#pragma unroll 1
+            for (int g = 1; g < KS; ++g) {
+                const float* src = mb + ((long long)((g - 1) * NMT + mt) * 32 + lane) * C::MERGE_FLOATS;
+                const float4 st = *reinterpret_cast<const float4*>(src + 4 * NT_O);
+                const float M0 = fmaxf(m0, st.x), M1 = fmaxf(m1, st.y);
+                const float a0 = m0 == NEG_INF ? 0.f : fast_exp2(m0 - M0);
+                const float a1 = m1 == NEG_INF ? 0.f : fast_exp2(m1 - M1);
+                const float b0 = st.x == NEG_INF ? 0.f : fast_exp2(st.x - M0);
+                const float b1 = st.y == NEG_INF ? 0.f : fast_exp2(st.y - M1);
+#pragma unroll
+                for (int i = 0; i < NT_O; ++i) {
+                    const float4 v = *reinterpret_cast<const float4*>(src + 4 * i);
+                    oacc[i][0] = oacc[i][0] * a0 + v.x * b0;
+                    oacc[i][1] = oacc[i][1] * a0 + v.y * b0;
+                    oacc[i][2] = oacc[i][2] * a1 + v.z * b1;
+                    oacc[i][3] = oacc[i][3] * a1 + v.w * b1;
+                }
+                l0 = l0 * a0 + st.z * b0;
+                l1 = l1 * a1 + st.w * b1;
+                m0 = M0;
+                m1 = M1;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(merge_empty);
+        }
         l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
         l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
@@ -520,26 +604,26 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE>::THREADS)
     }
 }
 
-template <int D, int PS, int NMT, bool SPARSE>
+template <int D, int PS, int NMT, bool SPARSE, int KS>
 int attn_ctas_per_sm_t() {
-    using C = AttnCfg<D, PS, NMT, SPARSE>;
+    using C = AttnCfg<D, PS, NMT, SPARSE, KS>;
     int n = 0;
     // The answer depends on the kernel's dynamic shared-memory limit: set it first
     // so the launch shape is the same before and after the kernel's first launch.
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, PS, NMT, SPARSE>,
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, PS, NMT, SPARSE, KS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<D, PS, NMT, SPARSE>, C::THREADS, C::SMEM);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<D, PS, NMT, SPARSE, KS>, C::THREADS, C::SMEM);
     if (e != cudaSuccess) return 1;
     return n > 0 ? n : 1;
 }
 
-template <int D, int PS, int NMT, bool SPARSE>
+template <int D, int PS, int NMT, bool SPARSE, int KS>
 cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           cudaStream_t st) {
-    using C = AttnCfg<D, PS, NMT, SPARSE>;
-    auto kern = attn_kernel<D, PS, NMT, SPARSE>;
-    const int per_sm = attn_ctas_per_sm_t<D, PS, NMT, SPARSE>();
+    using C = AttnCfg<D, PS, NMT, SPARSE, KS>;
+    auto kern = attn_kernel<D, PS, NMT, SPARSE, KS>;
+    const int per_sm = attn_ctas_per_sm_t<D, PS, NMT, SPARSE, KS>();
     const long long units = (long long)a.B * a.H_kv * a.num_splits;
     long long grid = (long long)a.num_sms * per_sm;
     if (grid > units) grid = units;

@@ -8,9 +8,9 @@ namespace spd {
 template <int D, int PS>
 static cudaError_t dense_mt(const AttnArgs& a, const CUtensorMap& k, const CUtensorMap& v, cudaStream_t st) {
     switch (attn_mtiles(a.T, a.H_q / a.H_kv)) {
-        case 1: return launch_attn_t<D, PS, 1, false>(a, k, v, st);
-        case 2: return launch_attn_t<D, PS, 2, false>(a, k, v, st);
-        default: return launch_attn_t<D, PS, 4, false>(a, k, v, st);
+        case 1: return launch_attn_t<D, PS, 1, false, 1>(a, k, v, st);
+        case 2: return launch_attn_t<D, PS, 2, false, 1>(a, k, v, st);
+        default: return launch_attn_t<D, PS, 4, false, 1>(a, k, v, st);
     }
 }
 
@@ -32,9 +32,9 @@ cudaError_t launch_dense_attn(const AttnArgs& a, const CUtensorMap& tmK, const C
 template <int D, int PS>
 static int occ_mt(int mtiles) {
     switch (mtiles) {
-        case 1: return attn_ctas_per_sm_t<D, PS, 1, false>();
-        case 2: return attn_ctas_per_sm_t<D, PS, 2, false>();
-        default: return attn_ctas_per_sm_t<D, PS, 4, false>();
+        case 1: return attn_ctas_per_sm_t<D, PS, 1, false, 1>();
+        case 2: return attn_ctas_per_sm_t<D, PS, 2, false, 1>();
+        default: return attn_ctas_per_sm_t<D, PS, 4, false, 1>();
     }
 }
 

@@ -8,9 +8,9 @@ namespace spd {
 template <int D>
 static cudaError_t sparse_ps(const AttnArgs& a, const CUtensorMap& k, const CUtensorMap& v, cudaStream_t st) {
     switch (a.ps) {
-        case 16: return launch_attn_t<D, 16, 1, true>(a, k, v, st);
-        case 32: return launch_attn_t<D, 32, 1, true>(a, k, v, st);
-        default: return launch_attn_t<D, 64, 1, true>(a, k, v, st);
+        case 16: return launch_attn_t<D, 16, 1, true, 2>(a, k, v, st);
+        case 32: return launch_attn_t<D, 32, 1, true, 2>(a, k, v, st);
+        default: return launch_attn_t<D, 64, 1, true, 2>(a, k, v, st);
     }
 }
 
@@ -23,9 +23,9 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, const CUtensorMap& tmK, const 
 template <int D>
 static int occ_sparse(int ps) {
     switch (ps) {
-        case 16: return attn_ctas_per_sm_t<D, 16, 1, true>();
-        case 32: return attn_ctas_per_sm_t<D, 32, 1, true>();
-        default: return attn_ctas_per_sm_t<D, 64, 1, true>();
+        case 16: return attn_ctas_per_sm_t<D, 16, 1, true, 2>();
+        case 32: return attn_ctas_per_sm_t<D, 32, 1, true, 2>();
+        default: return attn_ctas_per_sm_t<D, 64, 1, true, 2>();
     }
 }
 

@@ -11,16 +11,16 @@
 // query heads form one m16n8 MMA tile per 16 summary channels.  The bf16
 // products are exact in fp32; accumulation is fp32.
 //
-// Work layout: a persistent grid (two CTAs of 4 warps per SM).  All 16-page
+// Work layout: a persistent grid (three CTAs of 4 warps per SM).  All 16-page
 // tiles of all (sequence, KV head) rows are numbered in one sequence and every
 // warp takes an equal contiguous share, so the work is balanced to a tile.
 // The summaries are stored sequence-major, so a tile is one contiguous 8 KB
-// run: every warp owns a ring of shared-memory slots filled by one 1-D bulk
-// copy per tile (completion counted on the slot's mbarrier) several tiles
-// ahead of the MMAs.  The summary channels are assigned to MMA
-// k-slots in the order each thread reads them and the query operand uses the
-// same order (the contraction is a sum, so any common order is exact), so no
-// shuffles or ldmatrix are needed.
+// run: every warp owns a 2-slot ring of shared-memory slots filled by one 1-D
+// bulk copy per tile (completion counted on the slot's mbarrier) ahead of the
+// MMAs; many short rings stream better than a few deep ones.  The summary
+// channels are assigned to MMA k-slots in the order each thread reads them and
+// the query operand uses the same order (the contraction is a sum, so any
+// common order is exact), so no shuffles or ldmatrix are needed.
 //
 // Selection (a second kernel, one warp per (sequence, KV head) row): the
 // mandatory pages, then the k'-th best score by an 8-bit radix select over
@@ -35,7 +35,7 @@ namespace spd {
 
 constexpr int kScoreWarps = 4;
 constexpr int kScoreThreads = 32 * kScoreWarps;
-constexpr int kScoreStages = 3;
+constexpr int kScoreStages = 2;
 
 template <int D>
 struct ScoreCfg {
@@ -554,8 +554,8 @@ static cudaError_t launch_score_t(const ScoreSelectArgs& a, int grid, cudaStream
 
 cudaError_t launch_score_select(const ScoreSelectArgs& a, int num_sms, cudaStream_t st) {
     if (a.B == 0) return cudaSuccess;
-    // persistent: two CTAs per SM, each warp streams an equal share of all tiles
-    const int grid = 2 * num_sms;
+    // persistent: three CTAs per SM, each warp streams an equal share of all tiles
+    const int grid = 3 * num_sms;
     cudaError_t e = a.D == 128 ? launch_score_t<128>(a, grid, st) : launch_score_t<64>(a, grid, st);
     if (e != cudaSuccess) return e;
     // selection: one CTA per row, the row's keys in shared memory
