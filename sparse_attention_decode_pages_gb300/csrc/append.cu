@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(256) append_refresh_kernel(AppendArgs a) {
     const int warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
     const int b = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
     const int len = a.seq_lens[b];
     if (len < a.T || len > a.max_pages * a.ps) {
         if (threadIdx.x == 0 && blockIdx.y == 0) raise_status(a.status, SPD_DEV_BAD_LEN);
@@ -99,10 +101,8 @@ cudaError_t launch_append_refresh(const AppendArgs& a, cudaStream_t st) {
     const int warps = a.H_kv < 8 ? a.H_kv : 8;
     dim3 grid((unsigned)a.B, (unsigned)touched), block(32 * warps);
     if (a.D == 128)
-        append_refresh_kernel<128><<<grid, block, 0, st>>>(a);
-    else
-        append_refresh_kernel<64><<<grid, block, 0, st>>>(a);
-    return cudaGetLastError();
+        return launch_pdl(append_refresh_kernel<128>, grid, block, 0, st, a);
+    return launch_pdl(append_refresh_kernel<64>, grid, block, 0, st, a);
 }
 
 }  // namespace spd

@@ -121,7 +121,13 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
         }
         mbar_fence_init();
     }
+    if (tid == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
     __syncthreads();
+    pdl_wait();
+    pdl_trigger();
 
     // Output row r of a (b, h) row -> index into o ([B][T][H_q]) and lse.
     auto out_index = [&](int bh, int r) -> long long {
@@ -132,10 +138,6 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
 
     if (warp == C::CONSUMERS) {
         // ============================================================ producer warp
-        if (lane == 0) {
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-        }
         const long long total_units = (long long)a.B * a.H_kv * a.num_splits;
         int* queue = a.queue;  // [0..1] 64-bit unit counter, [2] producers finished
         long long j = 0;       // items issued
@@ -628,8 +630,7 @@ cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& tmK, const CUten
     long long grid = (long long)a.num_sms * per_sm;
     if (grid > units) grid = units;
     if (grid < 1) grid = 1;
-    kern<<<(unsigned)grid, C::THREADS, C::SMEM, st>>>(a, tmK, tmV);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, a, tmK, tmV);
 }
 
 }  // namespace spd

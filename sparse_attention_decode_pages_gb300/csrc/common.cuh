@@ -31,6 +31,14 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     return t;
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched so
+// that it may start while the previous kernel on the stream finishes; before
+// its first access to global memory it waits for that kernel (and so, in
+// turn, everything before it) to complete, and early on it lets the next
+// kernel start launching.  Both are no-ops without a programmatic dependency.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void raise_status(unsigned* status, unsigned bits) {
     if (status) atomicOr(status, bits);
 }

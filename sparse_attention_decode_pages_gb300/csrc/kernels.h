@@ -8,7 +8,28 @@
 
 #include "../../include/spd.h"
 
+#include <utility>
+
 namespace spd {
+
+// Launches a kernel of the library with programmatic stream serialisation
+// allowed (see pdl_wait / pdl_trigger): the launch of a kernel overlaps the
+// tail of the previous one on the stream.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 struct SummarizeArgs {
     const uint16_t* K;

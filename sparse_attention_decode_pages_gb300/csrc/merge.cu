@@ -12,6 +12,8 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(int S, int rows, int D, 
                                                         float* __restrict__ lse) {
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
     if (warp >= rows) return;
     const float NEG_INF = __int_as_float(0xff800000);
     float M = NEG_INF;
@@ -41,9 +43,8 @@ cudaError_t launch_lse_merge(int S, int rows, int D, const float* part_o, const 
     if (rows == 0) return cudaSuccess;
     const int warps_per_block = 8;
     const int blocks = (rows + warps_per_block - 1) / warps_per_block;
-    lse_merge_kernel<<<blocks, 32 * warps_per_block, 0, st>>>(S, rows, D, part_o, part_lse,
-                                                              reinterpret_cast<bf16*>(o), lse);
-    return cudaGetLastError();
+    return launch_pdl(lse_merge_kernel, dim3(blocks), dim3(32 * warps_per_block), 0, st, S, rows, D, part_o,
+                      part_lse, reinterpret_cast<bf16*>(o), lse);
 }
 
 }  // namespace spd

@@ -205,6 +205,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
     const unsigned lt_mask = (1u << lane) - 1u;
     const int row = blockIdx.x;
     const int b = row / a.H_kv;
+    pdl_wait();
+    pdl_trigger();
     const int len = a.seq_lens[b];
     const int P = (len + a.ps - 1) / a.ps;
     int32_t* out = a.sel + (long long)row * a.k_max;
@@ -401,6 +403,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
         for (int i = 0; i < kScoreStages; ++i) mbar_init(bars + i, 1);
         mbar_fence_init();
     }
+    pdl_wait();
+    pdl_trigger();
     // pref[b] = H_kv * (16-page tiles of sequences 0..b-1); a sequence's tiles are
     // ordered (KV head, tile).
     for (int bb = threadIdx.x; bb < a.B; bb += kScoreThreads) pages[bb] = (a.seq_lens[bb] + a.ps - 1) / a.ps;
@@ -548,8 +552,7 @@ static cudaError_t launch_score_t(const ScoreSelectArgs& a, int grid, cudaStream
     const size_t smem = 128 /*alignment slack*/ + 128 /*barriers*/ + ring + (2 * (size_t)a.B + 1) * sizeof(int);
     cudaError_t e = cudaFuncSetAttribute(score_select_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    score_select_kernel<D><<<grid, kScoreThreads, smem, st>>>(a, 0);
-    return cudaGetLastError();
+    return launch_pdl(score_select_kernel<D>, dim3(grid), dim3(kScoreThreads), smem, st, a, 0);
 }
 
 cudaError_t launch_score_select(const ScoreSelectArgs& a, int num_sms, cudaStream_t st) {
@@ -562,8 +565,7 @@ cudaError_t launch_score_select(const ScoreSelectArgs& a, int num_sms, cudaStrea
     const size_t smem = (size_t)a.max_pages * sizeof(uint32_t);
     e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    select_kernel<<<(unsigned)((long long)a.B * a.H_kv), kSelThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(select_kernel, dim3((unsigned)((long long)a.B * a.H_kv)), dim3(kSelThreads), smem, st, a);
 }
 
 }  // namespace spd

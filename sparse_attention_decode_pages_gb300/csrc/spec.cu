@@ -106,6 +106,8 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
     const int tpc = (ntiles + kSpecCluster - 1) / kSpecCluster;  // tiles per CTA
     u64* tsum = smem_w;
     u64* all = smem_w + tpc;
+    pdl_wait();
+    pdl_trigger();
 
     // the k <= 32 decisions in parallel, one lane each; the first rejection ends the run
     if (warp == 0) {
@@ -290,13 +292,12 @@ cudaError_t launch_spec_accept(const SpecArgs& a, cudaStream_t st) {
     if (a.n % 4 == 0) {
         e = cudaFuncSetAttribute(spec_accept_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        spec_accept_kernel<true><<<grid, kSpecThreads, smem, st>>>(a);
+        return launch_pdl(spec_accept_kernel<true>, dim3(grid), dim3(kSpecThreads), smem, st, a);
     } else {
         e = cudaFuncSetAttribute(spec_accept_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        spec_accept_kernel<false><<<grid, kSpecThreads, smem, st>>>(a);
+        return launch_pdl(spec_accept_kernel<false>, dim3(grid), dim3(kSpecThreads), smem, st, a);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace spd

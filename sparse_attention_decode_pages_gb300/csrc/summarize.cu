@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(256) summarize_kernel(SummarizeArgs a) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
+    pdl_wait();
+    pdl_trigger();
 
     int slot;
     if (a.only_pages) {
@@ -91,10 +93,8 @@ cudaError_t launch_summarize(const SummarizeArgs& a, cudaStream_t st) {
     const int warps = a.H_kv < 8 ? a.H_kv : 8;
     dim3 grid((unsigned)nblk), block(32 * warps);
     if (a.D == 128)
-        summarize_kernel<128><<<grid, block, 0, st>>>(a);
-    else
-        summarize_kernel<64><<<grid, block, 0, st>>>(a);
-    return cudaGetLastError();
+        return launch_pdl(summarize_kernel<128>, grid, block, 0, st, a);
+    return launch_pdl(summarize_kernel<64>, grid, block, 0, st, a);
 }
 
 }  // namespace spd
