@@ -4,10 +4,10 @@
 One step is one pass of the hot path over one batch (B = 64 sequences, 32 query
 / 8 KV heads, head dim 128, contexts 8K..16K, page size 16, budget 64 pages):
 
-  f1  the step's new token appended to each sequence's cache, with the
-      summary of its page rewritten (kv_append_refresh, T = 1; the a1
-      summaries of the rest of the cache are resident),
-  a2-a4  pages_score_select (upper-bound scores of every page, top-k budget),
+  f1-a4  pages_append_score_select: the step's new token appended to each
+      sequence's cache with the summary of its page rebuilt (f1, by the
+      scoring pass itself; the a1 summaries of the rest of the cache are
+      resident), upper-bound scores of every page and the top-k budget,
   a5-a6  sparse_decode_attn (split-K over the selected pages, fused merge),
   a7  dense_verify_attn of k+1 = 7 drafted positions over the full cache.
 
@@ -217,12 +217,10 @@ def run_gpu(args):
     def sparse_pass(ev=None):
         if ev:
             ev[0].record(stream)
-        spd.kv_append_refresh(dims, 1, d["K"], d["V"], d["page_table"], d["seq_lens"], k_new, v_new,
-                              summ)
-        if ev:
-            ev[1].record(stream)
-        spd.pages_score_select(dims, d["q"], summ, d["seq_lens"], policy, sel,
-                               nsel, k_max, ws_sel)
+        # f1 + a2-a4: the step's token appended (its page's summary rebuilt) by the
+        # scoring pass itself, then the selection
+        spd.pages_append_score_select(dims, d["K"], d["V"], d["page_table"], d["seq_lens"], k_new, v_new,
+                                      d["q"], summ, policy, sel, nsel, k_max, ws_sel)
         if ev:
             ev[2].record(stream)
         spd.sparse_decode_attn(dims, d["q"], d["K"], d["V"], d["page_table"], d["seq_lens"], sel,
@@ -259,7 +257,7 @@ def run_gpu(args):
     # in use); pass B puts events between the kernels (which serialises them)
     # for the per-kernel breakdown and the attention kernel's roofline.
     sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) if k != 1 else None for k in range(4)] for _ in range(args.steps)]
     vevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     sampler.start()
@@ -287,8 +285,7 @@ def run_gpu(args):
     if status:
         raise RuntimeError(f"device status {status:#x} in the timed region")
 
-    t_ref = [e[0].elapsed_time(e[1]) for e in evs]
-    t_sel = [e[1].elapsed_time(e[2]) for e in evs]
+    t_sel = [e[0].elapsed_time(e[2]) for e in evs]
     t_att = [e[2].elapsed_time(e[3]) for e in evs]
     t_step = [e[0].elapsed_time(e[1]) for e in sevs]
     t_step_serial = [e[0].elapsed_time(e[3]) for e in evs]
@@ -378,7 +375,7 @@ def run_gpu(args):
                 "splits": args.splits, "verify_splits": args.vsplits,
             },
             "step_ms": {"whole_step": ms_step, "serialised_step": float(np.mean(t_step_serial)),
-                        "f1_append_refresh": float(np.mean(t_ref)), "a2_a4_score_select": float(np.mean(t_sel)),
+                        "f1_a2_a4_append_score_select": float(np.mean(t_sel)),
                         "a5_a6_sparse_attn": ms_att},
             "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s",
                               "frac": step_gbs / peak, "bytes": nbytes["step"],
@@ -394,9 +391,9 @@ def run_gpu(args):
                              / (ms_ver * 1e-3) / 1e12},
             "e2e": {"value": world * w.B / (ms_e2e * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms": ms_e2e},
-            # pass A per step: append + refresh (f1), score + select (2), sparse attention
-            # with its fused merge (1), dense verification (1); pass B: the first four again
-            "gpu_launches": args.steps * 9,
+            # pass A per step: append + score (1), select (1), sparse attention with its
+            # fused merge (1), dense verification (1); pass B: the first three again
+            "gpu_launches": args.steps * 7,
             "clocks": clocks,
             "wall_s_timed_region": t1 - t0,
             "cpu_baseline": cpu,

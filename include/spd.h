@@ -217,6 +217,25 @@ spd_status pages_score_select(const spd_dims *dims, const spd_bf16 *q, const spd
                               void *stream);
 
 /*
+ * pages_append_score_select -- kv_append_refresh with T = 1 and
+ * pages_score_select in one pass over the summaries: the warp that scores the
+ * tile holding a row's last page first writes the step's token (position
+ * seq_lens[b] - 1) into K and V, rebuilds that page's summary (stored to summ
+ * and used for the score), then scores the tile.  Results (K, V, summ, sel,
+ * nsel, scores) are bit-identical to kv_append_refresh(T = 1) followed by
+ * pages_score_select; one kernel launch and one pass over the cache update
+ * fewer.  k_new, v_new: bf16 [B][H_kv][D].  A sequence with seq_lens[b] = 0
+ * sets SPD_DEV_BAD_LEN and is skipped; a page id outside [0, num_phys_pages)
+ * sets SPD_DEV_BAD_PAGE.  Other arguments and errors as the two calls.
+ */
+spd_status pages_append_score_select(const spd_dims *dims, spd_bf16 *K, spd_bf16 *V,
+                                     const int32_t *page_table, const int32_t *seq_lens,
+                                     const spd_bf16 *k_new, const spd_bf16 *v_new, const spd_bf16 *q,
+                                     spd_bf16 *summ, const spd_budget_policy *policy, int32_t *sel,
+                                     int32_t *nsel, int32_t k_max, float *scores, void *ws,
+                                     size_t ws_bytes, void *stream);
+
+/*
  * sparse_decode_attn -- attention of the decode query over the selected pages
  * only (block-sparse page attention: Sparrow, "Insights" and "Control Study
  * 2"; the S3R sparse drafter of Table 7).

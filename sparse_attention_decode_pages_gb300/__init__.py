@@ -107,6 +107,7 @@ def lib():
         L.lse_merge.argtypes = [i32, i32, i32, P, P, P, P, P]
         L.kv_append_refresh.argtypes = [DP, i32, P, P, P, P, P, P, P, P]
         L.spec_accept.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, P]
+        L.pages_append_score_select.argtypes = [DP, P, P, P, P, P, P, P, P, PP, P, P, i32, P, P, sz, P]
         L.spd_round_create.argtypes = [ctypes.POINTER(RoundDesc), ctypes.POINTER(ctypes.c_void_p)]
         L.spd_round_launch.argtypes = [P, i32, P]
         L.spd_round_destroy.argtypes = [P]
@@ -114,6 +115,7 @@ def lib():
         for f in ("spd_device_status", "pages_summarize", "pages_score_select",
                   "sparse_decode_attn", "dense_verify_attn", "lse_merge",
                   "sparse_decode_attn_noalloc", "kv_append_refresh", "spec_accept",
+                  "pages_append_score_select",
                   "spd_round_create", "spd_round_launch"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
@@ -203,6 +205,15 @@ def spec_accept(p_draft, q_target, draft, u_acc, u_res, n_accepted, tokens, stre
     B, k, n = p_draft.shape
     _check(lib().spec_accept(B, k, n, _ptr(p_draft), _ptr(q_target), _ptr(draft), _ptr(u_acc),
                              _ptr(u_res), _ptr(n_accepted), _ptr(tokens), _stream(stream)))
+
+
+def pages_append_score_select(dims: Dims, K, V, page_table, seq_lens, k_new, v_new, q, summ, policy,
+                              sel, nsel, k_max: int, ws, scores=None, stream=None):
+    pol = policy if isinstance(policy, Policy) else policy_of(policy)
+    _check(lib().pages_append_score_select(ctypes.byref(dims), _ptr(K), _ptr(V), _ptr(page_table),
+                                           _ptr(seq_lens), _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(summ),
+                                           ctypes.byref(pol), _ptr(sel), _ptr(nsel), k_max, _ptr(scores),
+                                           _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def pages_score_select(dims: Dims, q, summ, seq_lens, policy, sel, nsel, k_max: int, ws,

@@ -86,6 +86,14 @@ struct ScoreSelectArgs {
     int B, H_q, H_kv, D, ps, max_pages;
     long long num_phys;
     unsigned* status;
+    // Fused append (pages_append_score_select): the step's token, written into the
+    // cache and into its page's summary by the warp that scores that page.
+    uint16_t* K;  // NULL: no append
+    uint16_t* V;
+    const int32_t* page_table;
+    const uint16_t* k_new;  // [B][H_kv][D]
+    const uint16_t* v_new;
+    uint16_t* summ_w;       // == summ
 };
 // Scores every page (persistent grid sized to num_sms), then selects per row.
 cudaError_t launch_score_select(const ScoreSelectArgs& a, int num_sms, cudaStream_t st);

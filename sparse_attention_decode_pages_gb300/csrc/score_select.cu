@@ -211,7 +211,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
     const int P = (len + a.ps - 1) / a.ps;
     int32_t* out = a.sel + (long long)row * a.k_max;
     if (P <= 0) {
-        if (tid == 0) a.nsel[row] = 0;
+        if (tid == 0) {
+            a.nsel[row] = 0;
+            if (a.K) raise_status(a.status, SPD_DEV_BAD_LEN);  // no position for the fused append
+        }
         return;
     }
     const int sink = min(a.pol.sink_pages, P), local = min(a.pol.local_pages, P);
@@ -383,6 +386,75 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
     }
 }
 
+// Fused append of the step's token for row (b, h): the token at position
+// len - 1 is written into the K / V cache, the summary of its page is rebuilt
+// from the page's valid rows (the older ones read from the cache) and stored
+// both to global memory and into the shared-memory copy of the tile being
+// scored (`entry`, which the bulk copy filled with the stale summary).  Warp-
+// wide; the same arithmetic as kv_append_refresh, so the same bits.
+template <int D>
+__device__ void append_last_page(const ScoreSelectArgs& a, int b, int h, int len, int P, uint8_t* entry) {
+    constexpr int LPR = D * 2 / 16;  // lanes per row (16-byte chunks per row)
+    constexpr int RPI = 32 / LPR;    // rows per warp instruction
+    const int lane = threadIdx.x & 31;
+    const int lp = P - 1;
+    const int valid = len - lp * a.ps;  // rows of the page, the new token last
+    const long long phys = a.page_table[(long long)b * a.max_pages + lp];
+    if (phys < 0 || phys >= a.num_phys) {
+        if (lane == 0) raise_status(a.status, SPD_DEV_BAD_PAGE);
+        return;
+    }
+    const long long row0 = (phys * a.H_kv + h) * a.ps;
+    uint4* kt = reinterpret_cast<uint4*>(a.K + row0 * D);
+    uint4* vt = reinterpret_cast<uint4*>(a.V + row0 * D);
+    const int r0 = lane / LPR, ch = lane % LPR;
+    const __nv_bfloat162 pinf = __floats2bfloat162_rn(__int_as_float(0x7f800000), __int_as_float(0x7f800000));
+    const __nv_bfloat162 ninf = __floats2bfloat162_rn(__int_as_float(0xff800000), __int_as_float(0xff800000));
+    __nv_bfloat162 mn[4], mx[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        mn[i] = pinf;
+        mx[i] = ninf;
+    }
+    for (int t = r0; t < valid; t += RPI) {
+        uint4 k;
+        if (t == valid - 1) {
+            const long long src = ((long long)b * a.H_kv + h) * (D / 8);
+            k = __ldg(reinterpret_cast<const uint4*>(a.k_new) + src + ch);
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.v_new) + src + ch);
+            kt[t * LPR + ch] = k;
+            vt[t * LPR + ch] = v;
+        } else {
+            k = kt[t * LPR + ch];
+        }
+        const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&k);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            mn[i] = __hmin2(mn[i], e[i]);
+            mx[i] = __hmax2(mx[i], e[i]);
+        }
+    }
+#pragma unroll
+    for (int off = LPR; off < 32; off <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t a_ = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<uint32_t*>(&mn[i]), off);
+            uint32_t b_ = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<uint32_t*>(&mx[i]), off);
+            mn[i] = __hmin2(mn[i], *reinterpret_cast<__nv_bfloat162*>(&a_));
+            mx[i] = __hmax2(mx[i], *reinterpret_cast<__nv_bfloat162*>(&b_));
+        }
+    }
+    if (r0 == 0) {
+        uint4* out = reinterpret_cast<uint4*>(a.summ_w + (((long long)b * a.H_kv + h) * a.max_pages + lp) * 2LL * D);
+        out[ch] = *reinterpret_cast<uint4*>(mn);
+        out[LPR + ch] = *reinterpret_cast<uint4*>(mx);
+        reinterpret_cast<uint4*>(entry)[ch] = *reinterpret_cast<uint4*>(mn);
+        reinterpret_cast<uint4*>(entry)[LPR + ch] = *reinterpret_cast<uint4*>(mx);
+        // these generic writes precede the next bulk copy into the slot
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelectArgs a, int unused) {
     using C = ScoreCfg<D>;
@@ -488,6 +560,10 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
             break;
         }
         const uint8_t* sl = ring + slot * SLOT;
+        if (a.K && p0 <= P - 1 && P - 1 < p0 + 16) {  // this tile holds the row's last page
+            append_last_page<D>(a, b, h, a.seq_lens[b], P, ring + slot * SLOT + (P - 1 - p0) * C::PAGE_BYTES);
+            __syncwarp();
+        }
         if (row != cur_row) {
             // B fragments of this row's query heads: k-step 2j holds channels
             // 32j+8c+{0,1 | 2,3}, k-step 2j+1 holds +{4,5 | 6,7}

@@ -352,10 +352,10 @@ SPD_API spd_status spec_accept(int32_t B, int32_t k, int32_t n_vocab, const floa
     return e == cudaSuccess ? SPD_OK : cuda_fail(e, "spec_accept launch");
 }
 
-SPD_API spd_status pages_score_select(const spd_dims* dims, const spd_bf16* q, const spd_bf16* summ,
-                                      const int32_t* seq_lens,
-                                      const spd_budget_policy* policy, int32_t* sel, int32_t* nsel, int32_t k_max,
-                                      float* scores, void* ws, size_t ws_bytes, void* stream) {
+static spd_status score_select_setup(const spd_dims* dims, const spd_bf16* q, const spd_bf16* summ,
+                                     const int32_t* seq_lens, const spd_budget_policy* policy, int32_t* sel,
+                                     int32_t* nsel, int32_t k_max, float* scores, void* ws, size_t ws_bytes,
+                                     ScoreSelectArgs& a, DevInfo** dev) {
     spd_status st = check_dims(dims);
     if (st != SPD_OK) return st;
     if (!policy) return fail(SPD_ERR_INVALID_ARG, "policy is NULL");
@@ -385,7 +385,7 @@ SPD_API spd_status pages_score_select(const spd_dims* dims, const spd_bf16* q, c
     DevInfo* d = dev_info(&st);
     if (!d) return st;
     const long long rows = (long long)dims->B * dims->H_kv;
-    ScoreSelectArgs a;
+    a = ScoreSelectArgs{};
     a.q = q;
     a.summ = summ;
     a.seq_lens = seq_lens;
@@ -403,8 +403,43 @@ SPD_API spd_status pages_score_select(const spd_dims* dims, const spd_bf16* q, c
     a.max_pages = dims->max_pages_per_seq;
     a.num_phys = dims->num_phys_pages;
     a.status = d->status;
+    *dev = d;
+    return SPD_OK;
+}
+
+SPD_API spd_status pages_score_select(const spd_dims* dims, const spd_bf16* q, const spd_bf16* summ,
+                                      const int32_t* seq_lens,
+                                      const spd_budget_policy* policy, int32_t* sel, int32_t* nsel, int32_t k_max,
+                                      float* scores, void* ws, size_t ws_bytes, void* stream) {
+    ScoreSelectArgs a;
+    DevInfo* d = nullptr;
+    spd_status st = score_select_setup(dims, q, summ, seq_lens, policy, sel, nsel, k_max, scores, ws, ws_bytes, a, &d);
+    if (st != SPD_OK || dims->B == 0) return st;
     cudaError_t e = launch_score_select(a, d->sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SPD_OK : cuda_fail(e, "pages_score_select launch");
+}
+
+SPD_API spd_status pages_append_score_select(const spd_dims* dims, spd_bf16* K, spd_bf16* V,
+                                             const int32_t* page_table, const int32_t* seq_lens,
+                                             const spd_bf16* k_new, const spd_bf16* v_new, const spd_bf16* q,
+                                             spd_bf16* summ, const spd_budget_policy* policy, int32_t* sel,
+                                             int32_t* nsel, int32_t k_max, float* scores, void* ws,
+                                             size_t ws_bytes, void* stream) {
+    ScoreSelectArgs a;
+    DevInfo* d = nullptr;
+    spd_status st = score_select_setup(dims, q, summ, seq_lens, policy, sel, nsel, k_max, scores, ws, ws_bytes, a, &d);
+    if (st != SPD_OK || dims->B == 0) return st;
+    if (!K || !V || !page_table || !k_new || !v_new) return fail(SPD_ERR_INVALID_ARG, "NULL pointer argument");
+    if (!aligned16(K) || !aligned16(V) || !aligned16(k_new) || !aligned16(v_new))
+        return fail(SPD_ERR_INVALID_ARG, "K, V, k_new and v_new must be 16-byte aligned");
+    a.K = K;
+    a.V = V;
+    a.page_table = page_table;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.summ_w = summ;
+    cudaError_t e = launch_score_select(a, d->sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPD_OK : cuda_fail(e, "pages_append_score_select launch");
 }
 
 static spd_status attn_common(const spd_dims* dims, const spd_bf16* q, const spd_bf16* K, const spd_bf16* V,

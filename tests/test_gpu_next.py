@@ -252,3 +252,60 @@ def test_top_p_then_sparse_attention():
     assert g.sync_status() == 0
     o_ref, lse_ref = oracle.sparse_attn(w, sel.cpu().numpy(), nsel.cpu().numpy(), threads=8)
     assert_close_outputs(np_bf16(o), o_ref, lse.cpu().numpy(), lse_ref)
+
+
+# ---------------------------------------------------------------- f1 fused into scoring
+
+@pytest.mark.parametrize("name,kw", [("q8b", dict(B=6, len_lo=700, len_hi=2200)),
+                                     ("sweep", dict(page_size=32, B=3, len_lo=2000, len_hi=5000)),
+                                     ("sweep", dict(page_size=64, B=3, len_lo=2000, len_hi=5000)),
+                                     ("tiny", dict())])
+def test_fused_append_score_select_equals_the_two_calls(name, kw):
+    """pages_append_score_select gives the same bits as kv_append_refresh(T=1) then
+    pages_score_select: cache, summaries, scores and selection."""
+    import torch
+    import sparse_attention_decode_pages_gb300 as spd
+    w = wl.named(name, threads=4, **kw)
+    k_new, v_new = _new_tokens(w, 1, 21)
+    outs = []
+    for fused in (False, True):
+        g = Gpu(w)
+        summ = g.summarize()
+        kn = torch.from_numpy(k_new).view(torch.bfloat16).cuda()
+        vn = torch.from_numpy(v_new).view(torch.bfloat16).cuda()
+        sel = torch.full((w.B, w.H_kv, w.k_max), -1, dtype=torch.int32, device="cuda")
+        nsel = torch.full((w.B, w.H_kv), -7, dtype=torch.int32, device="cuda")
+        sc = torch.full((w.B, w.H_kv, w.max_pages_per_seq), float("nan"), device="cuda")
+        ws = g.ws(spd.spd_score_select_workspace_size(g.dims))
+        d = g.d
+        if fused:
+            spd.pages_append_score_select(g.dims, d["K"], d["V"], d["page_table"], d["seq_lens"], kn, vn,
+                                          d["q"], summ, w.policy, sel, nsel, w.k_max, ws, scores=sc)
+        else:
+            spd.kv_append_refresh(g.dims, 1, d["K"], d["V"], d["page_table"], d["seq_lens"], kn, vn, summ)
+            spd.pages_score_select(g.dims, d["q"], summ, d["seq_lens"], w.policy, sel, nsel, w.k_max, ws,
+                                   scores=sc)
+        assert g.sync_status() == 0
+        outs.append([_bits(d["K"]), _bits(d["V"]), summ_bits(summ), sel.cpu().numpy(), nsel.cpu().numpy(),
+                     sc.view(torch.int32).cpu().numpy()])
+    for x, y, what in zip(outs[0], outs[1], ["K", "V", "summ", "sel", "nsel", "scores"]):
+        assert np.array_equal(x, y), what
+
+
+def test_fused_append_flags_empty_sequences_and_bad_pages():
+    import torch
+    import sparse_attention_decode_pages_gb300 as spd
+    w = custom([0, 40, 50], 4, 2, 64, 16, rng=np.random.default_rng(3))
+    w.page_table[2, 3] = w.num_phys_pages + 9      # the last page of sequence 2
+    g = Gpu(w)
+    summ = torch.zeros((w.B, w.H_kv, w.max_pages_per_seq, 2, w.D), dtype=torch.bfloat16, device="cuda")
+    k_new, v_new = _new_tokens(w, 1, 4)
+    kn = torch.from_numpy(k_new).view(torch.bfloat16).cuda()
+    vn = torch.from_numpy(v_new).view(torch.bfloat16).cuda()
+    sel = torch.zeros((w.B, w.H_kv, w.k_max), dtype=torch.int32, device="cuda")
+    nsel = torch.zeros((w.B, w.H_kv), dtype=torch.int32, device="cuda")
+    ws = g.ws(spd.spd_score_select_workspace_size(g.dims))
+    d = g.d
+    spd.pages_append_score_select(g.dims, d["K"], d["V"], d["page_table"], d["seq_lens"], kn, vn, d["q"],
+                                  summ, w.policy, sel, nsel, w.k_max, ws)
+    assert g.sync_status() == 0x8 | 0x1
