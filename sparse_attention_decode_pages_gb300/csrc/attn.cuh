@@ -61,22 +61,22 @@ struct AttnCfg {
     // R <= RP); padding rows are zero in registers.
     static constexpr int QROWS = SPARSE ? 8 : RP;
     static constexpr int QBYTES = QROWS * D * 2;
-    // Q buffers per group: every unit spans >= KS items (it is padded to a
-    // multiple of KS), so at most STAGES / KS + 1 units have items in the ring.
-    static constexpr int NQ = STAGES / KS + 1;
-    static constexpr int FIFO = 8;  // unit-info entries (>= NQ)
+    // Q buffers (per group) and unit-info entries: double-buffered; the producer
+    // reuses one only after every consumer warp has read it (the qempty barriers).
+    static constexpr int NQ = 2;
+    static constexpr int FIFO = NQ;
     // Per consumer lane of groups 1..KS-1: its O fragments, then m0, m1, l0, l1.
     static constexpr int MERGE_FLOATS = 4 * (D / 8) + 4;
     static constexpr int MERGE = KS > 1 ? (KS - 1) * NMT * 32 * MERGE_FLOATS * 4 : 0;
     static constexpr int OFF_Q = STAGES * SLOT;
     static constexpr int OFF_MERGE = OFF_Q + NQ * KS * QBYTES;
-    static constexpr int OFF_BAR = OFF_MERGE + MERGE;  // full[STAGES], empty[STAGES], merge_full, merge_empty
-    static constexpr int OFF_FIFO = OFF_BAR + (2 * STAGES + 2) * 8;
+    // full[STAGES], empty[STAGES], merge_full, merge_empty, qempty[NQ]
+    static constexpr int OFF_BAR = OFF_MERGE + MERGE;
+    static constexpr int OFF_FIFO = OFF_BAR + (2 * STAGES + 2 + NQ) * 8;
     static constexpr int OFF_META = OFF_FIFO + FIFO * (int)sizeof(UnitInfo);  // int2 per slot
     static constexpr int BODY = OFF_META + STAGES * 8;
     static constexpr int SMEM = 1024 /*alignment slack*/ + BODY;
     static_assert(STAGES % KS == 0, "each ring slot must belong to one consumer group");
-    static_assert(NQ <= FIFO, "ring deeper than the unit buffers");
 };
 
 constexpr int kEndOfWork = -2;  // slot_meta.x: no more items
@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
     uint64_t* empty = full + STAGES;
     uint64_t* merge_full = empty + STAGES;  // groups 1..KS-1 have written their state
     uint64_t* merge_empty = merge_full + 1; // group 0 has read it
+    uint64_t* qempty = merge_empty + 1;     // [NQ]: every consumer warp has read unit info and Q
     UnitInfo* fifo = reinterpret_cast<UnitInfo*>(smem + C::OFF_FIFO);
     int2* slot_meta = reinterpret_cast<int2*>(smem + C::OFF_META);  // {logical page or -1 / end, unit seq}
 
@@ -119,6 +120,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
             mbar_init(merge_full, (KS - 1) * NMT);
             mbar_init(merge_empty, NMT);
         }
+        for (int i = 0; i < C::NQ; ++i) mbar_init(qempty + i, C::CONSUMERS);
         mbar_fence_init();
     }
     if (tid == 0) {
@@ -191,6 +193,15 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
                     }
                 continue;
             }
+            if (seq >= C::NQ) {  // the unit-info entry and Q buffer of unit seq - NQ must be free
+                bool r = true;
+                if (lane == 0)
+                    r = mbar_wait_bounded(qempty + seq % C::NQ, (uint32_t)(((seq / C::NQ) - 1) & 1), a.status);
+                if (!__shfl_sync(0xffffffffu, r ? 1 : 0, 0)) {
+                    ok = false;
+                    break;
+                }
+            }
             if (lane == 0) {
                 UnitInfo info;
                 info.row = row;
@@ -199,7 +210,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
                 info.count = count;
                 info.len = len;
                 info.nsplit = (n_items + a.items_per_split - 1) / a.items_per_split;
-                fifo[seq % C::FIFO] = info;  // published by the first item's arrive (release)
+                fifo[seq % C::NQ] = info;  // published by the first item's arrive (release)
             }
             // Items are issued in multiples of KS (padding items carry no page), so
             // every unit starts on group 0 and each group sees each unit.
@@ -315,7 +326,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
         if (meta.y != cur_seq) {
             // new unit: its info, Q fragments, fresh softmax state, row limits
             cur_seq = meta.y;
-            cu = fifo[cur_seq % C::FIFO];
+            cu = fifo[cur_seq % C::NQ];
             c_item = 0;
             g_items = (cu.count + KS - 1) / KS;
             const uint8_t* qsm = qbuf + ((cur_seq % C::NQ) * KS + kg) * C::QBYTES;
@@ -334,6 +345,8 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
             lim0 = qr0 < R ? cu.len - a.T + qr0 / G : cu.len - 1;
             lim1 = qr1 < R ? cu.len - a.T + qr1 / G : cu.len - 1;
             lim_min = cu.len - a.T;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qempty + cur_seq % C::NQ);  // done with unit info and Q
         }
         const int lp = meta.x;
         if (lp >= 0) {
