@@ -127,13 +127,30 @@ __device__ int top_p_pages(const ScoreSelectArgs& a, const uint32_t* keys, int P
         hist[tid] = 0;
         mhist[tid] = 0;
         __syncthreads();
-        for (int p = tid; p < P; p += kSelThreads) {
-            if (mand(p)) continue;
-            const uint32_t u = keys[p];
-            if ((u & pmask) != prefix) continue;
-            const uint32_t bin = (u >> shift) & 255u;
-            atomicAdd(hist + bin, 1u);
-            atomicAdd(mhist + bin, (u64)page_weight(u, smax, c2));
+        for (int p0 = 0; p0 < P; p0 += kSelThreads) {
+            const int p = p0 + tid;
+            bool in = false;
+            uint32_t bin = 0, w = 0;
+            if (p < P && !mand(p)) {
+                const uint32_t u = keys[p];
+                if ((u & pmask) == prefix) {
+                    in = true;
+                    bin = (u >> shift) & 255u;
+                    w = page_weight(u, smax, c2);
+                }
+            }
+            // neighbouring scores share bins: one pair of atomics per distinct bin in the
+            // warp (a weight is < 2^32, so its two 16-bit halves sum without overflow)
+            const unsigned act = __ballot_sync(0xffffffffu, in);
+            if (in) {
+                const unsigned same = __match_any_sync(act, bin);
+                const unsigned hi = __reduce_add_sync(same, w >> 16);
+                const unsigned lo = __reduce_add_sync(same, w & 0xffffu);
+                if (lane == __ffs(same) - 1) {
+                    atomicAdd(hist + bin, (uint32_t)__popc(same));
+                    atomicAdd(mhist + bin, ((u64)hi << 16) + (u64)lo);
+                }
+            }
         }
         __syncthreads();
         if (warp == 0) {

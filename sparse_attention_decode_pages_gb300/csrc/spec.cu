@@ -18,8 +18,10 @@
 // and slow: this part runs fp64 at a small fraction of its fp32 rate).
 //
 // The draw streams the row once.  Each CTA sums the 128-element tiles of its
-// share of the row, a warp per tile and two tiles in flight per warp, into its
-// shared memory.  After a cluster barrier, CTA 0 gathers every tile sum
+// share of the row into its shared memory: rows whose length is a multiple of
+// 4 arrive through a 2-deep ring of 16-tile chunks filled by bulk copies (each
+// warp sums two tiles of each chunk); other rows through plain loads, a warp
+// per tile.  Eight 8-warp CTAs per sequence fit in one wave at B = 64.  After a cluster barrier, CTA 0 gathers every tile sum
 // through distributed shared memory and block-scans contiguous runs of them;
 // the one thread whose run holds the target finds the crossing tile, and a
 // warp scans that tile's 128 weights to find the element.
@@ -32,10 +34,15 @@ namespace cg = cooperative_groups;
 
 namespace spd {
 
-constexpr int kSpecThreads = 512;
+constexpr int kSpecThreads = 256;
 constexpr int kSpecTile = 128;
 constexpr int kSpecCluster = 8;
 constexpr int kSpecUnroll = 2;
+// n % 4 == 0 rows stream through shared memory: chunks of 16 tiles (q and p),
+// kSpecStages in flight per CTA, copied by the bulk-copy engine.
+constexpr int kSpecChunk = 16 * kSpecTile;  // elements
+constexpr int kSpecStages = 2;
+constexpr size_t kSpecRingBytes = (size_t)kSpecStages * 2 * kSpecChunk * sizeof(float);
 typedef unsigned long long u64;
 
 // floor(2^40 v) from the float's bits, in integer operations only (a 64-bit
@@ -88,9 +95,10 @@ __device__ __forceinline__ u64 shfl_xor_u64(u64 v, int off) {
 }
 
 template <bool VEC>
-__global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThreads, 2)
+__global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThreads, 4)
     spec_accept_kernel(SpecArgs a) {
-    extern __shared__ u64 smem_w[];  // [tpc] own tile sums, then (CTA 0) [ntiles] all tile sums
+    // [VEC: ring of kSpecStages x {q, p} chunks][tpc own tile sums][(CTA 0) ntiles all tile sums][VEC: bars]
+    extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ int s_acc, s_bad, s_tok, s_cross_tile;
     __shared__ u64 s_cross_run;
     __shared__ u64 s_warp[kSpecThreads / 32];
@@ -104,8 +112,17 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
     const long long n = a.n;
     const int ntiles = (int)((n + kSpecTile - 1) / kSpecTile);
     const int tpc = (ntiles + kSpecCluster - 1) / kSpecCluster;  // tiles per CTA
-    u64* tsum = smem_w;
-    u64* all = smem_w + tpc;
+    float* ring = reinterpret_cast<float*>(smem_raw);
+    u64* tsum = reinterpret_cast<u64*>(smem_raw + (VEC ? kSpecRingBytes : 0));
+    u64* all = tsum + tpc;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(all + ntiles);
+    if (VEC && tid == 0) {
+        for (int i = 0; i < kSpecStages; ++i) mbar_init(bars + i, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    unsigned chunks_done = 0;  // ring phases used so far (VEC)
+    bool dead = false;         // a bounded wait ran out: skip the data, keep the protocol
     pdl_wait();
     pdl_trigger();
 
@@ -152,38 +169,74 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
         // attempt 0: the residual at a rejection, or the target row after k acceptances;
         // attempt 1 (after a rejection whose residual is zero everywhere): the target row
         const bool residual = (attempt == 0) && (acc < k);
-        for (int t = my0 + warp; t < my1; t += NW * kSpecUnroll) {
-            float4 q4[kSpecUnroll], p4[kSpecUnroll];
+        if (VEC) {
+            const long long e0 = (long long)my0 * kSpecTile;
+            const long long e1 = min((long long)my1 * kSpecTile, n);
+            const int nchunks = e1 > e0 ? (int)((e1 - e0 + kSpecChunk - 1) / kSpecChunk) : 0;
+            auto issue = [&](int c) {  // thread 0
+                const int slot = (int)((chunks_done + c) % kSpecStages);
+                const long long s0 = e0 + (long long)c * kSpecChunk;
+                const uint32_t nb = (uint32_t)(min((long long)kSpecChunk, e1 - s0) * sizeof(float));
+                float* dst = ring + (size_t)slot * 2 * kSpecChunk;
+                mbar_arrive_expect_tx(bars + slot, residual ? 2 * nb : nb);
+                bulk_load(dst, qr + s0, nb, bars + slot);
+                if (residual) bulk_load(dst + kSpecChunk, pr + s0, nb, bars + slot);
+            };
+            if (tid == 0)
+                for (int c = 0; c < kSpecStages && c < nchunks; ++c) issue(c);
+            for (int c = 0; c < nchunks; ++c) {
+                const int slot = (int)((chunks_done + c) % kSpecStages);
+                if (!dead && !mbar_wait_bounded(bars + slot, ((chunks_done + c) / kSpecStages) & 1u, a.status))
+                    dead = true;
+                // warp w sums tiles w, w + NW, ... of the chunk
+                const long long s0 = e0 + (long long)c * kSpecChunk;
 #pragma unroll
-            for (int u = 0; u < kSpecUnroll; ++u) {
-                const int tt = t + u * NW;
-                const long long x0 = (long long)tt * kSpecTile + lane * 4;
-                q4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                p4[u] = q4[u];
-                if (tt < my1) {
-                    if (VEC && x0 + 4 <= n) {
-                        q4[u] = __ldg(reinterpret_cast<const float4*>(qr + x0));
-                        if (residual) p4[u] = __ldg(reinterpret_cast<const float4*>(pr + x0));
-                    } else {
-                        float qv[4] = {0.f, 0.f, 0.f, 0.f}, pv[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int tw = warp; tw < kSpecChunk / kSpecTile; tw += NW) {
+                    const long long x0 = s0 + (long long)tw * kSpecTile + lane * 4;
+                    u64 sum = 0;
+                    if (!dead && x0 < e1) {
+                        const float* src = ring + (size_t)slot * 2 * kSpecChunk + tw * kSpecTile + lane * 4;
+                        const float4 q4 = *reinterpret_cast<const float4*>(src);
+                        const float4 p4 = residual ? *reinterpret_cast<const float4*>(src + kSpecChunk)
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                        sum = spec_w(q4.x, p4.x, residual) + spec_w(q4.y, p4.y, residual) +
+                              spec_w(q4.z, p4.z, residual) + spec_w(q4.w, p4.w, residual);
+                    }
+#pragma unroll
+                    for (int off = 16; off; off >>= 1) sum += shfl_xor_u64(sum, off);
+                    const int t = (int)((s0 - e0) / kSpecTile) + tw;
+                    if (lane == 0 && t < my1 - my0) tsum[t] = sum;
+                }
+                __syncthreads();  // the slot has been read
+                if (tid == 0 && c + kSpecStages < nchunks) issue(c + kSpecStages);
+            }
+            chunks_done += nchunks;
+        } else {
+            for (int t = my0 + warp; t < my1; t += NW * kSpecUnroll) {
+                float4 q4[kSpecUnroll], p4[kSpecUnroll];
+#pragma unroll
+                for (int u = 0; u < kSpecUnroll; ++u) {
+                    const int tt = t + u * NW;
+                    const long long x0 = (long long)tt * kSpecTile + lane * 4;
+                    float qv[4] = {0.f, 0.f, 0.f, 0.f}, pv[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (tt < my1)
                         for (int j = 0; j < 4 && x0 + j < n; ++j) {
                             qv[j] = __ldg(qr + x0 + j);
                             if (residual) pv[j] = __ldg(pr + x0 + j);
                         }
-                        q4[u] = make_float4(qv[0], qv[1], qv[2], qv[3]);
-                        p4[u] = make_float4(pv[0], pv[1], pv[2], pv[3]);
-                    }
+                    q4[u] = make_float4(qv[0], qv[1], qv[2], qv[3]);
+                    p4[u] = make_float4(pv[0], pv[1], pv[2], pv[3]);
                 }
-            }
 #pragma unroll
-            for (int u = 0; u < kSpecUnroll; ++u) {
-                const int tt = t + u * NW;
-                if (tt >= my1) break;  // warp-uniform
-                u64 s = spec_w(q4[u].x, p4[u].x, residual) + spec_w(q4[u].y, p4[u].y, residual) +
-                        spec_w(q4[u].z, p4[u].z, residual) + spec_w(q4[u].w, p4[u].w, residual);
+                for (int u = 0; u < kSpecUnroll; ++u) {
+                    const int tt = t + u * NW;
+                    if (tt >= my1) break;  // warp-uniform
+                    u64 sum = spec_w(q4[u].x, p4[u].x, residual) + spec_w(q4[u].y, p4[u].y, residual) +
+                              spec_w(q4[u].z, p4[u].z, residual) + spec_w(q4[u].w, p4[u].w, residual);
 #pragma unroll
-                for (int off = 16; off; off >>= 1) s += shfl_xor_u64(s, off);
-                if (lane == 0) tsum[tt - my0] = s;
+                    for (int off = 16; off; off >>= 1) sum += shfl_xor_u64(sum, off);
+                    if (lane == 0) tsum[tt - my0] = sum;
+                }
             }
         }
         __syncthreads();
@@ -281,7 +334,8 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
 size_t spec_smem_bytes(long long n) {
     const long long ntiles = (n + kSpecTile - 1) / kSpecTile;
     const long long tpc = (ntiles + kSpecCluster - 1) / kSpecCluster;
-    return (size_t)(tpc + ntiles) * sizeof(u64);
+    const size_t ring = n % 4 == 0 ? kSpecRingBytes : 0;
+    return ring + (size_t)(tpc + ntiles) * sizeof(u64) + kSpecStages * sizeof(uint64_t);
 }
 
 cudaError_t launch_spec_accept(const SpecArgs& a, cudaStream_t st) {
