@@ -59,6 +59,27 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def replica_seed(base_seed: int, rank: int) -> int:
+    """Each rank of a multi-GPU run is an independent replica with its own seeded batch."""
+    return base_seed + 100 * rank
+
+
+def max_over_ranks(values, world: int, device):
+    """The per-rank timings reduced to their maximum over ranks (the slowest replica
+    sets the job's time); a no-op on one rank."""
+    import torch
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_tokens_per_s(world: int, batch: int, ms: float) -> float:
+    """Whole-job throughput: every replica processes its own batch in `ms`."""
+    return world * batch / (ms * 1e-3)
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -169,7 +190,7 @@ def run_gpu(args):
 
     # Each rank is an independent replica with its own seeded batch.
     spec = wl.spec(args.config, args.page_size)
-    spec.seed += 100 * rank
+    spec.seed = replica_seed(spec.seed, rank)
     if args.batch:
         spec.B = args.batch
     w = wl.make(spec)
@@ -326,10 +347,7 @@ def run_gpu(args):
                                               reps=max(10, min(args.steps, 50)), warmup=args.warmup)
 
     # max over ranks
-    vals = torch.tensor([ms_step, ms_ver, float(np.mean(e2e_ms)), ms_att], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    ms_step, ms_ver, ms_e2e, ms_att = [float(x) for x in vals.tolist()]
+    ms_step, ms_ver, ms_e2e, ms_att = max_over_ranks([ms_step, ms_ver, float(np.mean(e2e_ms)), ms_att], world, dev)
 
     peak, peak_src = hbm_peak()
     att_gbs = nbytes["attn"] / (ms_att * 1e-3) / 1e9
@@ -351,7 +369,7 @@ def run_gpu(args):
             cpu = cpu_baseline(w, T)
         line = {
             "metric": METRIC,
-            "value": world * w.B / (ms_step * 1e-3),
+            "value": job_tokens_per_s(world, w.B, ms_step),
             "unit": "tokens/s",
             "n_gpus": world,
             "steps": args.steps,
@@ -389,7 +407,7 @@ def run_gpu(args):
                              "achieved_gbs": ver_gbs, "frac": ver_gbs / peak, "bytes": vbytes,
                              "tflops": 4.0 * sum(int(w.seq_lens[b]) for b in range(w.B)) * w.H_q * T * w.D
                              / (ms_ver * 1e-3) / 1e12},
-            "e2e": {"value": world * w.B / (ms_e2e * 1e-3), "unit": "tokens/s",
+            "e2e": {"value": job_tokens_per_s(world, w.B, ms_e2e), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms": ms_e2e},
             # pass A per step: append + score (1), select (1), sparse attention with its
             # fused merge (1), dense verification (1); pass B: the first three again

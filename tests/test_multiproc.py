@@ -1,0 +1,73 @@
+"""The benchmark's multi-replica logic on CPU: two gloo ranks (world size 2).
+
+The path has no data exchange (every (sequence, KV head) is independent), so
+several GPUs run independent replicas; what the ranks share is the timing
+reduction (the slowest replica sets the job time), the per-rank seeds and the
+rank-0-only output of the reference arm."""
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def _rank_main(rank, world, port, out):
+    import torch
+    import torch.distributed as dist
+    import bench
+    from sparse_attention_decode_pages_gb300 import workloads as wl
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local = [1.0 + rank, 5.0 - rank, 2.5 * (rank + 1)]
+        got = bench.max_over_ranks(local, world, torch.device("cpu"))
+        spec = wl.spec("tiny")
+        spec.seed = bench.replica_seed(spec.seed, rank)
+        w = wl.make(spec)
+        qsum = float(np.asarray(w.q, dtype=np.float64).sum())
+        dist.barrier()
+        out.put((rank, got, spec.seed, qsum, bench.job_tokens_per_s(world, w.B, got[0])))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_reduce_timings_and_use_distinct_batches():
+    world, port = 2, 29500 + os.getpid() % 1000
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = dict((r, (g, s, qs, v)) for r, g, s, qs, v in (q.get(timeout=120) for _ in range(world)))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    # every rank sees the maximum over ranks of each timing
+    assert res[0][0] == res[1][0] == [2.0, 5.0, 5.0]
+    # replicas draw different batches from different seeds
+    assert res[0][1] != res[1][1] and res[0][2] != res[1][2]
+    # the job's throughput counts both replicas' batches over the slowest time
+    assert res[0][3] == pytest.approx(2 * 2 / 2.0e-3)
+
+
+def test_reference_arm_prints_on_rank_zero_only():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3", "--config", "tiny"], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_reference_arm_line_on_rank_zero():
+    import json
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
+                        "--warmup", "3", "--config", "tiny"], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-500:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["higher_is_better"] is True
