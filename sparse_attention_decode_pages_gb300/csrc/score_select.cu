@@ -22,12 +22,15 @@
 // the query operand uses the same order (the contraction is a sum, so any
 // common order is exact), so no shuffles or ldmatrix are needed.
 //
-// Selection (a second kernel, one warp per (sequence, KV head) row): the
+// Selection (a second kernel, one CTA per (sequence, KV head) row): the
 // mandatory pages, then the k'-th best score by an 8-bit radix select over
-// order-preserving uint32 keys (4 passes; shared-memory histogram with
-// warp-aggregated atomics, since neighbouring scores share their high bytes),
-// and pages above it plus the lowest-id pages equal to it, compacted in
-// ascending order into sel[] with ballots.
+// order-preserving uint32 keys (shared-memory histogram with warp-aggregated
+// atomics, since neighbouring scores share their high bytes).  As soon as the
+// digit being refined holds at most 256 keys (after two passes, typically),
+// those keys are ranked pairwise by (key desc, page asc) instead; otherwise the
+// four passes end on the exact k'-th key.  Pages above the boundary plus the
+// boundary pages that rank (or, at an exact key, the lowest-id pages equal to
+// it) are compacted in ascending order into sel[] with ballots.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -58,6 +61,9 @@ __device__ __forceinline__ long long budget_pages(const spd_budget_policy& pol, 
 
 constexpr int kSelWarps = 8;
 constexpr int kSelThreads = 32 * kSelWarps;
+// Once the radix digit being refined holds at most this many candidates, they
+// are ranked directly (pairwise) instead of refining further digits.
+constexpr int kRankMax = kSelThreads;
 
 __device__ __forceinline__ float key_float(uint32_t u) {
     return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
@@ -216,8 +222,11 @@ __device__ int top_p_pages(const ScoreSelectArgs& a, const uint32_t* keys, int P
 __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) {
     extern __shared__ uint32_t keys[];
     __shared__ uint32_t hist[256];
-    __shared__ int s_digit, s_rem;
+    __shared__ int s_digit, s_rem, s_cnt, s_ncol;
     __shared__ int w_eq[kSelWarps], w_take[kSelWarps];
+    __shared__ uint32_t col_key[kRankMax];
+    __shared__ int col_p[kRankMax];
+    __shared__ uint32_t s_chosen[32768 / 32];  // boundary pages chosen by rank (bit per page)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned lt_mask = (1u << lane) - 1u;
     const int row = blockIdx.x;
@@ -268,6 +277,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
 
     uint32_t thr;
     int rem;
+    // ranked: the boundary digit's candidates were ranked; chosen ones are in s_chosen
+    bool ranked = false;
+    uint32_t prefix = 0, pmask = 0;
     if (kp <= 0) {
         thr = 0xffffffffu;
         rem = 0;
@@ -275,7 +287,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
         thr = 0u;
         rem = ncand;
     } else {
-        uint32_t prefix = 0, pmask = 0;
         rem = kp;
         for (int shift = 24; shift >= 0; shift -= 8) {
             hist[tid] = 0;  // kSelThreads == 256 bins
@@ -320,6 +331,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
                         if (cum + (int)cnt[i] >= rem) {
                             s_digit = 255 - 8 * lane - i;
                             s_rem = rem - cum;
+                            s_cnt = (int)cnt[i];
                             break;
                         }
                         cum += (int)cnt[i];
@@ -330,8 +342,40 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
             prefix |= (uint32_t)s_digit << shift;
             pmask |= 255u << shift;
             rem = s_rem;
+            if (shift > 0 && s_cnt <= kRankMax) {  // few enough: rank them (block-uniform)
+                ranked = true;
+                break;
+            }
         }
         thr = prefix;
+    }
+    if (ranked) {
+        // The candidates whose key matches the refined prefix, ranked by (key desc,
+        // page asc); the first `rem` of them are chosen.
+        for (int w = tid; w < (P + 31) / 32; w += kSelThreads) s_chosen[w] = 0u;
+        if (tid == 0) s_ncol = 0;
+        __syncthreads();
+        for (int p = tid; p < P; p += kSelThreads) {
+            if (mand(p)) continue;
+            const uint32_t u = keys[p];
+            if ((u & pmask) != prefix) continue;
+            const int at = atomicAdd(&s_ncol, 1);
+            col_key[at] = u;  // at < s_cnt <= kRankMax
+            col_p[at] = p;
+        }
+        __syncthreads();
+        const int m = s_ncol;
+        if (tid < m) {
+            const uint32_t ki = col_key[tid];
+            const int pi = col_p[tid];
+            int r = 0;
+            for (int j = 0; j < m; ++j) {
+                const uint32_t kj = col_key[j];
+                r += (kj > ki) || (kj == ki && col_p[j] < pi);
+            }
+            if (r < rem) atomicOr(&s_chosen[pi >> 5], 1u << (pi & 31));
+        }
+        __syncthreads();
     }
 
     // Ascending compaction: mandatory pages, keys above the threshold, and the
@@ -339,10 +383,21 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
     // segment of pages; per-warp counts are scanned through shared memory.
     const int seg = ((P + kSelWarps * 32 - 1) / (kSelWarps * 32)) * 32;
     const int lo = min(P, warp * seg), hi = min(P, lo + seg);
+    auto pick = [&](int p, bool& m, bool& eq) -> bool {  // taken regardless of tie order?
+        m = mand(p);
+        eq = false;
+        if (m) return true;
+        const uint32_t u = keys[p];
+        if (ranked) return (u & pmask) > prefix || ((s_chosen[p >> 5] >> (p & 31)) & 1u);
+        eq = u == thr;
+        return u > thr;
+    };
     int n_eq = 0;
     for (int p0 = lo; p0 < hi; p0 += 32) {
         const int p = p0 + lane;
-        n_eq += __popc(__ballot_sync(0xffffffffu, p < hi && !mand(p) && keys[p] == thr));
+        bool m = false, eq = false;
+        if (p < hi) pick(p, m, eq);
+        n_eq += __popc(__ballot_sync(0xffffffffu, eq));
     }
     if (lane == 0) w_eq[warp] = n_eq;
     __syncthreads();
@@ -353,17 +408,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
         int eqb = eq_before;
         for (int p0 = lo; p0 < hi; p0 += 32) {
             const int p = p0 + lane;
-            bool m = false, eq = false, gt = false;
-            if (p < hi) {
-                m = mand(p);
-                if (!m) {
-                    const uint32_t u = keys[p];
-                    eq = u == thr;
-                    gt = u > thr;
-                }
-            }
+            bool m = false, eq = false, sure = false;
+            if (p < hi) sure = pick(p, m, eq);
             const unsigned eb = __ballot_sync(0xffffffffu, eq);
-            const bool take = m || gt || (eq && eqb + __popc(eb & lt_mask) < rem);
+            const bool take = sure || (eq && eqb + __popc(eb & lt_mask) < rem);
             n_take += __popc(__ballot_sync(0xffffffffu, take));
             eqb += __popc(eb);
         }
@@ -379,17 +427,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
         int eqb = eq_before;
         for (int p0 = lo; p0 < hi; p0 += 32) {
             const int p = p0 + lane;
-            bool m = false, eq = false, gt = false;
-            if (p < hi) {
-                m = mand(p);
-                if (!m) {
-                    const uint32_t u = keys[p];
-                    eq = u == thr;
-                    gt = u > thr;
-                }
-            }
+            bool m = false, eq = false, sure = false;
+            if (p < hi) sure = pick(p, m, eq);
             const unsigned eb = __ballot_sync(0xffffffffu, eq);
-            const bool take = m || gt || (eq && eqb + __popc(eb & lt_mask) < rem);
+            const bool take = sure || (eq && eqb + __popc(eb & lt_mask) < rem);
             const unsigned tb = __ballot_sync(0xffffffffu, take);
             const int at = pos + __popc(tb & lt_mask);
             if (take && at < a.k_max) out[at] = p;
