@@ -2,12 +2,13 @@
 """Benchmark: sparse paged decode attention on the Qwen3-8B-shaped workload.
 
 One step is one pass of the hot path over one batch (B = 64 sequences, 32 query
-/ 8 KV heads, head dim 128, contexts 8K..16K, page size 16, budget 64 pages):
+/ 8 KV heads, head dim 128, contexts 8K..16K, page size 16, budget 64 pages),
+timed as one sparse_decode_step call (the three kernels chained row by row):
 
-  f1-a4  pages_append_score_select: the step's new token appended to each
-      sequence's cache with the summary of its page rebuilt (f1, by the
-      scoring pass itself; the a1 summaries of the rest of the cache are
-      resident), upper-bound scores of every page and the top-k budget,
+  f1-a4  the step's new token appended to each sequence's cache with the
+      summary of its page rebuilt (f1, by the scoring pass itself; the a1
+      summaries of the rest of the cache are resident), upper-bound scores of
+      every page and the top-k budget,
   a5-a6  sparse_decode_attn (split-K over the selected pages, fused merge),
   a7  dense_verify_attn of k+1 = 7 drafted positions over the full cache.
 
@@ -235,7 +236,14 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
     policy = spd.policy_of(w.policy)
 
+    ws_step = spd.workspace(spd.spd_sparse_decode_step_workspace_size(dims, k_max), dev)
+
     def sparse_pass(ev=None):
+        if ev is None and args.splits == 0:
+            # the whole step in one call: append, score + select and attention chained row by row
+            spd.sparse_decode_step(dims, d["K"], d["V"], d["page_table"], d["seq_lens"], k_new, v_new, d["q"],
+                                   summ, policy, sel, nsel, k_max, o, ws_step, lse=lse)
+            return
         if ev:
             ev[0].record(stream)
         # f1 + a2-a4: the step's token appended (its page's summary rebuilt) by the
@@ -388,8 +396,9 @@ def run_gpu(args):
                 "global_batch": world * w.B,
                 "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                 "l2": "evicted between timed passes by reading a 512 MiB buffer (outside the events)",
-                "timing": "value from whole-step events (kernels overlap their launches); the per-kernel "
-                          "breakdown and the roofline from a second pass with events between the kernels",
+                "timing": "value from whole-step events around sparse_decode_step (its kernels chained row by "
+                          "row); the per-kernel breakdown and the roofline from a second pass of the separate "
+                          "calls with events between them",
                 "splits": args.splits, "verify_splits": args.vsplits,
             },
             "step_ms": {"whole_step": ms_step, "serialised_step": float(np.mean(t_step_serial)),

@@ -255,6 +255,32 @@ spd_status sparse_decode_attn(const spd_dims *dims, const spd_bf16 *q, const spd
                               spd_bf16 *o, float *lse, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * sparse_decode_step -- one whole sparse decode step in one call: the step's
+ * token appended (as kv_append_refresh with T = 1; skipped when k_new and
+ * v_new are NULL), every page scored and the budgeted selection made (as
+ * pages_score_select), and attention over the selected pages (as
+ * sparse_decode_attn with automatic splits).  Results -- K, V, summ, sel,
+ * nsel, o, lse -- are those of the separate calls.
+ *
+ * When every (sequence, KV head) row is one attention unit (enough rows to
+ * occupy the GPU, e.g. B = 64 at 8 KV heads), the three kernels are chained
+ * row by row instead of grid by grid: scoring hands out its tiles in row order
+ * and counts the finished tiles of each row, the selection of a row starts as
+ * soon as its count is complete, and the attention of a row as soon as its
+ * selection is published (release / acquire flags in the workspace; every
+ * wait is bounded and reports SPD_DEV_TIMEOUT).  Otherwise the calls run one
+ * after the other.  The workspace (spd_sparse_decode_step_workspace_size
+ * bytes) must be zero before its first use and is left zero; calls that
+ * overlap on the GPU need separate workspaces.  Errors as the separate calls.
+ */
+size_t spd_sparse_decode_step_workspace_size(const spd_dims *dims, int32_t k_max);
+spd_status sparse_decode_step(const spd_dims *dims, spd_bf16 *K, spd_bf16 *V, const int32_t *page_table,
+                              const int32_t *seq_lens, const spd_bf16 *k_new, const spd_bf16 *v_new,
+                              const spd_bf16 *q, spd_bf16 *summ, const spd_budget_policy *policy,
+                              int32_t *sel, int32_t *nsel, int32_t k_max, float softmax_scale,
+                              spd_bf16 *o, float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/*
  * sparse_decode_attn_noalloc -- sparse_decode_attn for callers that cannot
  * allocate device memory.  It has no counterpart on the pages: it is the same
  * computation, with the same arguments and results as sparse_decode_attn,

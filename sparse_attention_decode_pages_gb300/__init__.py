@@ -108,6 +108,10 @@ def lib():
         L.kv_append_refresh.argtypes = [DP, i32, P, P, P, P, P, P, P, P]
         L.spec_accept.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, P]
         L.pages_append_score_select.argtypes = [DP, P, P, P, P, P, P, P, P, PP, P, P, i32, P, P, sz, P]
+        L.spd_sparse_decode_step_workspace_size.argtypes = [DP, i32]
+        L.spd_sparse_decode_step_workspace_size.restype = sz
+        L.sparse_decode_step.argtypes = [DP, P, P, P, P, P, P, P, P, PP, P, P, i32, ctypes.c_float, P, P,
+                                         P, sz, P]
         L.spd_round_create.argtypes = [ctypes.POINTER(RoundDesc), ctypes.POINTER(ctypes.c_void_p)]
         L.spd_round_launch.argtypes = [P, i32, P]
         L.spd_round_destroy.argtypes = [P]
@@ -115,7 +119,7 @@ def lib():
         for f in ("spd_device_status", "pages_summarize", "pages_score_select",
                   "sparse_decode_attn", "dense_verify_attn", "lse_merge",
                   "sparse_decode_attn_noalloc", "kv_append_refresh", "spec_accept",
-                  "pages_append_score_select",
+                  "pages_append_score_select", "sparse_decode_step",
                   "spd_round_create", "spd_round_launch"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
@@ -214,6 +218,20 @@ def pages_append_score_select(dims: Dims, K, V, page_table, seq_lens, k_new, v_n
                                            _ptr(seq_lens), _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(summ),
                                            ctypes.byref(pol), _ptr(sel), _ptr(nsel), k_max, _ptr(scores),
                                            _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def spd_sparse_decode_step_workspace_size(dims: Dims, k_max: int) -> int:
+    return _size(lib().spd_sparse_decode_step_workspace_size(ctypes.byref(dims), k_max), "decode step workspace")
+
+
+def sparse_decode_step(dims: Dims, K, V, page_table, seq_lens, k_new, v_new, q, summ, policy, sel, nsel,
+                       k_max: int, o, ws, lse=None, softmax_scale: float | None = None, stream=None):
+    pol = policy if isinstance(policy, Policy) else policy_of(policy)
+    scale = 1.0 / math.sqrt(dims.D) if softmax_scale is None else softmax_scale
+    _check(lib().sparse_decode_step(ctypes.byref(dims), _ptr(K), _ptr(V), _ptr(page_table), _ptr(seq_lens),
+                                    _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(summ), ctypes.byref(pol), _ptr(sel),
+                                    _ptr(nsel), k_max, scale, _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
+                                    _stream(stream)))
 
 
 def pages_score_select(dims: Dims, q, summ, seq_lens, policy, sel, nsel, k_max: int, ws,

@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
         tma_prefetch_desc(&tmV);
     }
     __syncthreads();
-    pdl_wait();
+    if (!a.sel_done) pdl_wait();  // chained step: each unit waits for its row's selection instead
     pdl_trigger();
 
     // Output row r of a (b, h) row -> index into o ([B][T][H_q]) and lse.
@@ -166,6 +166,23 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
             const int row = (int)(u / a.num_splits), split = (int)(u % a.num_splits);
             const int b = row / a.H_kv, h = row - b * a.H_kv;
             const int start = split * a.items_per_split;
+            if (SPARSE && a.sel_done) {
+                // chained step: wait for the row's selection flag; then every lane
+                // acquires it (so its own loads below are ordered after the
+                // selection's writes) and the TMA issuer fences the async proxy
+                bool okw = true;
+                if (lane == 0) okw = flag_wait_bounded(a.sel_done + row, 1u, a.status);
+                if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) {
+                    ok = false;
+                    break;
+                }
+                (void)ld_acquire(a.sel_done + row);
+                __syncwarp();
+                if (lane == 0) {
+                    a.sel_done[row] = 0u;  // consumed (one unit per row in a chained step)
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
+            }
             // The first 32 selection entries are loaded together with the length
             // and the count (one round trip instead of two).
             int pre = -1;

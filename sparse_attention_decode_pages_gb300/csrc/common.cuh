@@ -39,6 +39,10 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Waits (bounded, like the mbarrier waits) until *flag >= value, with acquire
+// semantics at GPU scope; false (and SPD_DEV_TIMEOUT) if it never happens.
+__device__ __forceinline__ bool flag_wait_bounded(const unsigned* flag, unsigned value, unsigned* status);
+
 __device__ __forceinline__ void raise_status(unsigned* status, unsigned bits) {
     if (status) atomicOr(status, bits);
 }
@@ -90,6 +94,29 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            raise_status(status, SPD_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ bool flag_wait_bounded(const unsigned* flag, unsigned value, unsigned* status) {
+    if (ld_acquire(flag) >= value) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(128);
+        if (ld_acquire(flag) >= value) return true;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             raise_status(status, SPD_DEV_TIMEOUT);
             return false;

@@ -94,6 +94,13 @@ struct ScoreSelectArgs {
     const uint16_t* k_new;  // [B][H_kv][D]
     const uint16_t* v_new;
     uint16_t* summ_w;       // == summ
+    // Chained step (sparse_decode_step): tiles are handed out in row order from a
+    // counter, each finished tile is counted per row, and the selection of a row
+    // starts when its count is complete (instead of after the whole scoring grid).
+    unsigned long long* tile_ctr;  // NULL: static partition of the tiles
+    unsigned* warps_done;
+    unsigned* tiles_done;          // [B*H_kv], zero on entry and on exit
+    unsigned* sel_done;            // [B*H_kv]: set when a row's selection is written
 };
 // Scores every page (persistent grid sized to num_sms), then selects per row.
 cudaError_t launch_score_select(const ScoreSelectArgs& a, int num_sms, cudaStream_t st);
@@ -117,6 +124,7 @@ struct AttnArgs {
     int* queue;       // 16 bytes (8-aligned): unit queue + finished workers, zero on entry and exit
     int num_sms;
     unsigned* status;
+    unsigned* sel_done;  // chained step: wait for the row's selection flag instead of the previous grid
 };
 // Rows (T * G) handled per CTA, padded to 16-row MMA tiles.
 inline int attn_mtiles(int T, int G) {

@@ -39,6 +39,7 @@ namespace spd {
 constexpr int kScoreWarps = 4;
 constexpr int kScoreThreads = 32 * kScoreWarps;
 constexpr int kScoreStages = 2;
+constexpr int kChunkTiles = 4;  // chained step: tiles taken from the counter at a time
 
 template <int D>
 struct ScoreCfg {
@@ -231,8 +232,28 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
     const unsigned lt_mask = (1u << lane) - 1u;
     const int row = blockIdx.x;
     const int b = row / a.H_kv;
-    pdl_wait();
-    pdl_trigger();
+    __shared__ int s_ok;
+    if (a.tiles_done) {
+        // chained step: wait for this row's tiles only, not for the whole scoring grid
+        pdl_trigger();
+        if (tid == 0) {
+            const int P0 = (a.seq_lens[b] + a.ps - 1) / a.ps;
+            s_ok = flag_wait_bounded(a.tiles_done + row, (unsigned)((P0 + 15) / 16), a.status);
+            if (s_ok) a.tiles_done[row] = 0u;  // this row's count is consumed
+        }
+        __syncthreads();
+        if (!s_ok) return;
+    } else {
+        pdl_wait();
+        pdl_trigger();
+    }
+    // chained step: the row's selection is published to the attention kernel
+    auto publish = [&]() {
+        if (!a.sel_done) return;
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) st_release(a.sel_done + row, 1u);
+    };
     const int len = a.seq_lens[b];
     const int P = (len + a.ps - 1) / a.ps;
     int32_t* out = a.sel + (long long)row * a.k_max;
@@ -241,6 +262,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
             a.nsel[row] = 0;
             if (a.K) raise_status(a.status, SPD_DEV_BAD_LEN);  // no position for the fused append
         }
+        publish();
         return;
     }
     const int sink = min(a.pol.sink_pages, P), local = min(a.pol.local_pages, P);
@@ -442,6 +464,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
         if (total > a.k_max) raise_status(a.status, SPD_DEV_BAD_SEL);
         a.nsel[row] = min(total, a.k_max);
     }
+    publish();
 }
 
 // Fused append of the step's token for row (b, h): the token at position
@@ -560,7 +583,45 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
     const long long nwarps = (long long)gridDim.x * kScoreWarps;
     const long long gw = (long long)blockIdx.x * kScoreWarps + warp;
     const long long g0 = total * gw / nwarps, g1 = total * (gw + 1) / nwarps;
-    const int ntile = (int)(g1 - g0);
+    // The warp's t-th tile: its t-th of an equal contiguous share, or (chained step)
+    // the next tile in row order from the shared counter, so that rows finish in
+    // order and their selection can start while later rows are still scored.
+    // Chained step: chunks of kChunkTiles consecutive tiles are taken from the counter
+    // (rows finish in order), and a warp reports finished tiles to their row once
+    // per chunk (or row change), behind one fence.
+    bool drained = false;
+    long long ch_cur = 0, ch_end = 0;
+    auto grab = [&](int t) -> long long {
+        if (!a.tile_ctr) return g0 + t < g1 ? g0 + t : -1;
+        if (ch_cur < ch_end) return ch_cur++;
+        if (drained) return -1;
+        unsigned long long v = 0;
+        if (lane == 0) {
+            v = atomicAdd(a.tile_ctr, (unsigned long long)kChunkTiles);
+            if ((long long)v >= total) {  // each warp fails exactly once; the last one resets
+                if (atomicAdd(a.warps_done, 1u) == (unsigned)nwarps - 1) {
+                    *a.tile_ctr = 0ull;
+                    *a.warps_done = 0u;
+                }
+            }
+        }
+        v = __shfl_sync(0xffffffffu, v, 0);
+        if ((long long)v >= total) {
+            drained = true;
+            return -1;
+        }
+        ch_cur = (long long)v + 1;
+        ch_end = min((long long)v + kChunkTiles, total);
+        return (long long)v;
+    };
+    int pend_row = -1, pend_cnt = 0;  // tiles finished but not yet reported
+    auto report = [&]() {
+        if (pend_cnt == 0) return;
+        __threadfence();  // this warp's score (and append) stores before the count
+        __syncwarp();
+        if (lane == 0) atomicAdd(a.tiles_done + pend_row, (unsigned)pend_cnt);
+        pend_cnt = 0;
+    };
 
     // tile index -> (sequence, KV head, first page); shared-memory lookups only
     auto locate = [&](long long g, int& b, int& h, int& p0, int& P) {
@@ -578,9 +639,9 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
         p0 = (local - h * tb) * 16;
     };
     int issued_row = -1;
-    auto issue = [&](int t) {
+    auto issue = [&](int t, long long g) {
         int b, h, p0, P;
-        locate(g0 + t, b, h, p0, P);
+        locate(g, b, h, p0, P);
         const int row = b * a.H_kv + h;
         const bool newq = row != issued_row;
         issued_row = row;
@@ -597,24 +658,30 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
                                                           ((long long)b * a.H_q + h * G) * D * 2 + lane * 128));
     };
     __syncwarp();
+    long long gq[kScoreStages];
 #pragma unroll
-    for (int i = 0; i < kScoreStages; ++i)
-        if (i < ntile) issue(i);
+    for (int i = 0; i < kScoreStages; ++i) {
+        gq[i] = grab(i);
+        if (gq[i] >= 0) issue(i, gq[i]);
+    }
 
     uint32_t bq[NSS][4];
     int cur_row = -1;
     const int r = lane >> 2;
     const float ninf = __int_as_float(0xff800000);
     const bool h0 = 2 * c < G, h1 = 2 * c + 1 < G;
-    for (int t = 0; t < ntile; ++t) {
-        int b, h, p0, P;
-        locate(g0 + t, b, h, p0, P);
-        const int row = b * a.H_kv + h;
+    for (int t = 0;; ++t) {
         const int slot = t % kScoreStages;
+        const long long g = gq[slot];
+        if (g < 0) break;  // tiles are grabbed in order: every earlier one is done
+        int b, h, p0, P;
+        locate(g, b, h, p0, P);
+        const int row = b * a.H_kv + h;
         if (!mbar_wait_bounded(bars + slot, (uint32_t)((t / kScoreStages) & 1), a.status)) {
             // Let the copies still in flight land (bounded) before giving up.
-            for (int k2 = t + 1; k2 < ntile && k2 < t + kScoreStages; ++k2)
-                mbar_wait_bounded(bars + (k2 % kScoreStages), (uint32_t)((k2 / kScoreStages) & 1), a.status);
+            for (int k2 = t + 1; k2 < t + kScoreStages; ++k2)
+                if (gq[k2 % kScoreStages] >= 0)
+                    mbar_wait_bounded(bars + (k2 % kScoreStages), (uint32_t)((k2 / kScoreStages) & 1), a.status);
             break;
         }
         const uint8_t* sl = ring + slot * SLOT;
@@ -674,8 +741,18 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
             if (p0 + r + 8 < P) sc_row[p0 + r + 8] = s1;
         }
         __syncwarp();  // the slot has been read by every lane
-        if (t + kScoreStages < ntile) issue(t + kScoreStages);
+        if (a.tiles_done) {
+            if (row != pend_row) {
+                report();
+                pend_row = row;
+            }
+            ++pend_cnt;
+            if ((g + 1) % kChunkTiles == 0 || g + 1 == total) report();  // end of a chunk
+        }
+        gq[slot] = grab(t + kScoreStages);
+        if (gq[slot] >= 0) issue(t + kScoreStages, gq[slot]);
     }
+    if (a.tiles_done) report();
 }
 
 template <int D>

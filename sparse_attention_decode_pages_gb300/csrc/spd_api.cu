@@ -451,21 +451,14 @@ static spd_status attn_common(const spd_dims* dims, const spd_bf16* q, const spd
     return SPD_OK;
 }
 
-SPD_API spd_status sparse_decode_attn(const spd_dims* dims, const spd_bf16* q, const spd_bf16* K,
-                                      const spd_bf16* V, const int32_t* page_table, const int32_t* seq_lens,
-                                      const int32_t* sel, const int32_t* nsel, int32_t k_max, int32_t num_splits,
-                                      float softmax_scale, spd_bf16* o, float* lse, void* ws, size_t ws_bytes,
-                                      void* stream) {
-    spd_status st = check_dims(dims);
-    if (st != SPD_OK) return st;
-    if (k_max < 1) return fail(SPD_ERR_INVALID_ARG, "k_max < 1");
-    if (num_splits < 0) return fail(SPD_ERR_INVALID_ARG, "num_splits < 0");
-    if (dims->B == 0) return SPD_OK;
-    if ((st = attn_common(dims, q, K, V, page_table, seq_lens, o)) != SPD_OK) return st;
-    if (!sel || !nsel) return fail(SPD_ERR_INVALID_ARG, "NULL selection");
-    DevInfo* d = dev_info(&st);
-    if (!d) return st;
-    const int S = sparse_splits(dims, k_max, num_splits, d->sms);
+// Validates and launches the sparse attention kernel with S splits (S >= 1 already
+// chosen); sel_done != NULL chains it behind the selection of each row.
+static spd_status sparse_attn_launch(const spd_dims* dims, const spd_bf16* q, const spd_bf16* K, const spd_bf16* V,
+                                     const int32_t* page_table, const int32_t* seq_lens, const int32_t* sel,
+                                     const int32_t* nsel, int32_t k_max, int S, float softmax_scale, spd_bf16* o,
+                                     float* lse, void* ws, size_t ws_bytes, unsigned* sel_done, DevInfo* d,
+                                     void* stream) {
+    spd_status st;
     const int G = dims->H_q / dims->H_kv;
     const long long rows = (long long)dims->B * dims->H_kv;
     AttnWs w = attn_ws_layout(ws, rows, S, G, dims->D);
@@ -473,7 +466,7 @@ SPD_API spd_status sparse_decode_attn(const spd_dims* dims, const spd_bf16* q, c
     if (!aligned16(ws)) return fail(SPD_ERR_INVALID_ARG, "ws must be 16-byte aligned");
     CUtensorMap tk, tv;
     if ((st = kv_map(&tk, K, dims)) != SPD_OK || (st = kv_map(&tv, V, dims)) != SPD_OK) return st;
-    AttnArgs a;
+    AttnArgs a{};
     a.q = q;
     a.page_table = page_table;
     a.seq_lens = seq_lens;
@@ -499,8 +492,107 @@ SPD_API spd_status sparse_decode_attn(const spd_dims* dims, const spd_bf16* q, c
     a.queue = w.queue;
     a.num_sms = d->sms;
     a.status = d->status;
+    a.sel_done = sel_done;
     cudaError_t e = launch_sparse_attn(a, tk, tv, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? SPD_OK : cuda_fail(e, "sparse_decode_attn launch");
+    return e == cudaSuccess ? SPD_OK : cuda_fail(e, "sparse attention launch");
+}
+
+SPD_API spd_status sparse_decode_attn(const spd_dims* dims, const spd_bf16* q, const spd_bf16* K,
+                                      const spd_bf16* V, const int32_t* page_table, const int32_t* seq_lens,
+                                      const int32_t* sel, const int32_t* nsel, int32_t k_max, int32_t num_splits,
+                                      float softmax_scale, spd_bf16* o, float* lse, void* ws, size_t ws_bytes,
+                                      void* stream) {
+    spd_status st = check_dims(dims);
+    if (st != SPD_OK) return st;
+    if (k_max < 1) return fail(SPD_ERR_INVALID_ARG, "k_max < 1");
+    if (num_splits < 0) return fail(SPD_ERR_INVALID_ARG, "num_splits < 0");
+    if (dims->B == 0) return SPD_OK;
+    if ((st = attn_common(dims, q, K, V, page_table, seq_lens, o)) != SPD_OK) return st;
+    if (!sel || !nsel) return fail(SPD_ERR_INVALID_ARG, "NULL selection");
+    DevInfo* d = dev_info(&st);
+    if (!d) return st;
+    const int S = sparse_splits(dims, k_max, num_splits, d->sms);
+    return sparse_attn_launch(dims, q, K, V, page_table, seq_lens, sel, nsel, k_max, S, softmax_scale, o, lse, ws,
+                              ws_bytes, nullptr, d, stream);
+}
+
+// The chained step's workspace: [score / select][chain: tile counter, warps done,
+// tiles_done[rows], sel_done[rows]][attention].
+struct StepWs {
+    size_t score, chain, attn, bytes;
+};
+
+static bool step_ws_layout(const spd_dims* dims, int32_t k_max, StepWs* w, DevInfo* d) {
+    const long long rows = (long long)dims->B * dims->H_kv;
+    const int S = sparse_splits(dims, k_max, 0, d->sms);
+    w->score = align256(spd_score_select_workspace_size(dims));
+    w->chain = align256(16 + 2 * (size_t)rows * sizeof(unsigned));
+    w->attn = attn_ws_layout(nullptr, rows, S, dims->H_q / dims->H_kv, dims->D).bytes;
+    w->bytes = w->score + w->chain + w->attn;
+    return w->score != 0;
+}
+
+SPD_API size_t spd_sparse_decode_step_workspace_size(const spd_dims* dims, int32_t k_max) {
+    if (check_dims(dims) != SPD_OK) return 0;
+    if (k_max < 1) {
+        fail(SPD_ERR_INVALID_ARG, "k_max < 1");
+        return 0;
+    }
+    spd_status st = SPD_OK;
+    DevInfo* d = dev_info(&st);
+    if (!d) return 0;
+    StepWs w;
+    return step_ws_layout(dims, k_max, &w, d) ? w.bytes : 0;
+}
+
+SPD_API spd_status sparse_decode_step(const spd_dims* dims, spd_bf16* K, spd_bf16* V, const int32_t* page_table,
+                                      const int32_t* seq_lens, const spd_bf16* k_new, const spd_bf16* v_new,
+                                      const spd_bf16* q, spd_bf16* summ, const spd_budget_policy* policy,
+                                      int32_t* sel, int32_t* nsel, int32_t k_max, float softmax_scale,
+                                      spd_bf16* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
+    spd_status st = check_dims(dims);
+    if (st != SPD_OK) return st;
+    if (k_max < 1) return fail(SPD_ERR_INVALID_ARG, "k_max < 1");
+    if (dims->B == 0) return SPD_OK;
+    if ((k_new == nullptr) != (v_new == nullptr)) return fail(SPD_ERR_INVALID_ARG, "k_new and v_new: both or neither");
+    if ((st = attn_common(dims, q, K, V, page_table, seq_lens, o)) != SPD_OK) return st;
+    DevInfo* d = dev_info(&st);
+    if (!d) return st;
+    StepWs w;
+    if (!step_ws_layout(dims, k_max, &w, d)) return fail(SPD_ERR_INVALID_ARG, "bad dims");
+    if (!ws || ws_bytes < w.bytes) return fail(SPD_ERR_WORKSPACE, "workspace %zu bytes < %zu", ws_bytes, w.bytes);
+    if (!aligned16(ws)) return fail(SPD_ERR_INVALID_ARG, "ws must be 16-byte aligned");
+    char* base = static_cast<char*>(ws);
+    ScoreSelectArgs a;
+    DevInfo* d2 = nullptr;
+    st = score_select_setup(dims, q, summ, seq_lens, policy, sel, nsel, k_max, nullptr, base, w.score, a, &d2);
+    if (st != SPD_OK) return st;
+    if (k_new) {
+        if (!aligned16(k_new) || !aligned16(v_new)) return fail(SPD_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+        a.K = K;
+        a.V = V;
+        a.page_table = page_table;
+        a.k_new = k_new;
+        a.v_new = v_new;
+        a.summ_w = summ;
+    }
+    // Chained when every row is one attention unit: the selection of a row starts as
+    // soon as its tiles are scored and its attention as soon as it is selected.
+    const int S = sparse_splits(dims, k_max, 0, d->sms);
+    unsigned* sel_done = nullptr;
+    if (S == 1) {
+        char* chain = base + w.score;
+        const long long rows = (long long)dims->B * dims->H_kv;
+        a.tile_ctr = reinterpret_cast<unsigned long long*>(chain);
+        a.warps_done = reinterpret_cast<unsigned*>(chain + 8);
+        a.tiles_done = reinterpret_cast<unsigned*>(chain + 16);
+        a.sel_done = a.tiles_done + rows;
+        sel_done = a.sel_done;
+    }
+    cudaError_t e = launch_score_select(a, d->sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sparse_decode_step scoring launch");
+    return sparse_attn_launch(dims, q, K, V, page_table, seq_lens, sel, nsel, k_max, S, softmax_scale, o, lse,
+                              base + w.score + w.chain, w.attn, sel_done, d, stream);
 }
 
 SPD_API spd_status dense_verify_attn(const spd_dims* dims, int32_t T, const spd_bf16* q, const spd_bf16* K,
@@ -523,7 +615,7 @@ SPD_API spd_status dense_verify_attn(const spd_dims* dims, int32_t T, const spd_
     if (!aligned16(ws)) return fail(SPD_ERR_INVALID_ARG, "ws must be 16-byte aligned");
     CUtensorMap tk, tv;
     if ((st = kv_map(&tk, K, dims)) != SPD_OK || (st = kv_map(&tv, V, dims)) != SPD_OK) return st;
-    AttnArgs a;
+    AttnArgs a{};
     a.q = q;
     a.page_table = page_table;
     a.seq_lens = seq_lens;
@@ -641,7 +733,7 @@ SPD_API spd_status sparse_decode_attn_noalloc(const spd_dims* dims, const spd_bf
     const size_t zero_bytes = reinterpret_cast<char*>(w.part_lse) - static_cast<char*>(scratch);
     cudaError_t e = cudaMemsetAsync(scratch, 0, zero_bytes, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "clearing the fixed scratch array");
-    AttnArgs a;
+    AttnArgs a{};
     a.q = q;
     a.page_table = page_table;
     a.seq_lens = seq_lens;

@@ -79,6 +79,9 @@ def test_validation_rejects_bad_shapes_without_touching_the_gpu(libspd):
                                None) == 1                   # NULL pointers
     assert L.pages_append_score_select(ctypes.byref(d), None, None, None, None, None, None, None, None,
                                        ctypes.byref(pol), None, None, 8, None, None, 0, None) == 1
+    assert L.sparse_decode_step(ctypes.byref(d), None, None, None, None, None, None, None, None,
+                                ctypes.byref(pol), None, None, 8, ctypes.c_float(0.1), None, None, None, 0,
+                                None) == 1
     assert L.spec_accept(4, 0, 100, None, None, None, None, None, None, None, None) == 2   # k = 0
     assert L.spec_accept(4, 33, 100, None, None, None, None, None, None, None, None) == 2  # k > 32
     assert L.spec_accept(4, 6, 0, None, None, None, None, None, None, None, None) == 2    # empty vocab

@@ -309,3 +309,56 @@ def test_fused_append_flags_empty_sequences_and_bad_pages():
     spd.pages_append_score_select(g.dims, d["K"], d["V"], d["page_table"], d["seq_lens"], kn, vn, d["q"],
                                   summ, w.policy, sel, nsel, w.k_max, ws)
     assert g.sync_status() == 0x8 | 0x1
+
+
+# ---------------------------------------------------------------- the chained decode step
+
+@pytest.mark.parametrize("name,kw,append", [
+    ("q8b", dict(), True),                                              # full size: chained rows
+    ("q8b", dict(B=5, len_lo=700, len_hi=2200), True),                  # few rows: calls in turn
+    ("q17b", dict(B=48, len_lo=2000, len_hi=6000), False),
+    ("longtail", dict(B=2, len_lo=4000, len_hi=9000, T=1), True)])
+def test_decode_step_equals_the_separate_calls(name, kw, append):
+    """sparse_decode_step gives the bits of append + score_select + sparse attention, for
+    two steps in a row with different queries through one workspace (so the chain's
+    counters must have been reset by the first)."""
+    import torch
+    import sparse_attention_decode_pages_gb300 as spd
+    w = wl.named(name, threads=8, **kw)
+    k_new, v_new = _new_tokens(w, 1, 31)
+    rng = np.random.default_rng(32)
+    q2 = torch.from_numpy(wl.f32_to_bf16_bits(rng.standard_normal(w.q.shape).astype(np.float32))).view(
+        torch.bfloat16).cuda()
+    outs = []
+    for fused in (False, True):
+        g = Gpu(w)
+        summ = g.summarize()
+        d = g.d
+        kn = torch.from_numpy(k_new).view(torch.bfloat16).cuda() if append else None
+        vn = torch.from_numpy(v_new).view(torch.bfloat16).cuda() if append else None
+        sel = torch.full((w.B, w.H_kv, w.k_max), -1, dtype=torch.int32, device="cuda")
+        nsel = torch.full((w.B, w.H_kv), -7, dtype=torch.int32, device="cuda")
+        o = torch.full((w.B, w.H_q, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((w.B, w.H_q), float("nan"), device="cuda")
+        ws = g.ws(spd.spd_sparse_decode_step_workspace_size(g.dims, w.k_max))
+        wss = g.ws(spd.spd_score_select_workspace_size(g.dims))
+        wsa = g.ws(spd.spd_sparse_decode_workspace_size(g.dims, w.k_max, 0))
+        res = []
+        for q in (d["q"], q2):
+            if fused:
+                spd.sparse_decode_step(g.dims, d["K"], d["V"], d["page_table"], d["seq_lens"], kn, vn, q,
+                                       summ, w.policy, sel, nsel, w.k_max, o, ws, lse=lse)
+            else:
+                if append:
+                    spd.kv_append_refresh(g.dims, 1, d["K"], d["V"], d["page_table"], d["seq_lens"], kn, vn,
+                                          summ)
+                spd.pages_score_select(g.dims, q, summ, d["seq_lens"], w.policy, sel, nsel, w.k_max, wss)
+                spd.sparse_decode_attn(g.dims, q, d["K"], d["V"], d["page_table"], d["seq_lens"], sel, nsel,
+                                       w.k_max, o, wsa, lse=lse)
+            assert g.sync_status() == 0
+            res += [_bits(d["K"]), summ_bits(summ), sel.cpu().numpy(), nsel.cpu().numpy(), _bits(o),
+                    lse.view(torch.int32).cpu().numpy()]
+        outs.append(res)
+    names = ["K", "summ", "sel", "nsel", "o", "lse"] * 2
+    for x, y, what in zip(outs[0], outs[1], names):
+        assert np.array_equal(x, y), what
