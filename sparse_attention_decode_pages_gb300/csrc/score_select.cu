@@ -227,7 +227,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
     __shared__ int w_eq[kSelWarps], w_take[kSelWarps];
     __shared__ uint32_t col_key[kRankMax];
     __shared__ int col_p[kRankMax];
-    __shared__ uint32_t s_chosen[32768 / 32];  // boundary pages chosen by rank (bit per page)
+    // after the keys: boundary pages chosen by rank, and the final decision (bit per page)
+    uint32_t* s_chosen = keys + a.max_pages;
+    uint32_t* s_take = s_chosen + (a.max_pages + 31) / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned lt_mask = (1u << lane) - 1u;
     const int row = blockIdx.x;
@@ -414,17 +416,20 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
         eq = u == thr;
         return u > thr;
     };
-    int n_eq = 0;
-    for (int p0 = lo; p0 < hi; p0 += 32) {
-        const int p = p0 + lane;
-        bool m = false, eq = false;
-        if (p < hi) pick(p, m, eq);
-        n_eq += __popc(__ballot_sync(0xffffffffu, eq));
-    }
-    if (lane == 0) w_eq[warp] = n_eq;
-    __syncthreads();
     int eq_before = 0;
-    for (int w = 0; w < warp; ++w) eq_before += w_eq[w];
+    if (!ranked) {  // ties at an exact key are taken in page order: count them per warp
+        int n_eq = 0;
+        for (int p0 = lo; p0 < hi; p0 += 32) {
+            const int p = p0 + lane;
+            bool m = false, eq = false;
+            if (p < hi) pick(p, m, eq);
+            n_eq += __popc(__ballot_sync(0xffffffffu, eq));
+        }
+        if (lane == 0) w_eq[warp] = n_eq;
+        __syncthreads();
+        for (int w = 0; w < warp; ++w) eq_before += w_eq[w];
+    }
+    // decide every page once; the decisions (one word per 32 pages) are kept for the write
     int n_take = 0;
     {
         int eqb = eq_before;
@@ -434,7 +439,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
             if (p < hi) sure = pick(p, m, eq);
             const unsigned eb = __ballot_sync(0xffffffffu, eq);
             const bool take = sure || (eq && eqb + __popc(eb & lt_mask) < rem);
-            n_take += __popc(__ballot_sync(0xffffffffu, take));
+            const unsigned tb = __ballot_sync(0xffffffffu, take);
+            if (lane == 0) s_take[p0 >> 5] = tb;
+            n_take += __popc(tb);
             eqb += __popc(eb);
         }
     }
@@ -445,20 +452,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
         if (w < warp) pos += w_take[w];
         total += w_take[w];
     }
-    {
-        int eqb = eq_before;
-        for (int p0 = lo; p0 < hi; p0 += 32) {
-            const int p = p0 + lane;
-            bool m = false, eq = false, sure = false;
-            if (p < hi) sure = pick(p, m, eq);
-            const unsigned eb = __ballot_sync(0xffffffffu, eq);
-            const bool take = sure || (eq && eqb + __popc(eb & lt_mask) < rem);
-            const unsigned tb = __ballot_sync(0xffffffffu, take);
-            const int at = pos + __popc(tb & lt_mask);
-            if (take && at < a.k_max) out[at] = p;
-            pos += __popc(tb);
-            eqb += __popc(eb);
-        }
+    for (int p0 = lo; p0 < hi; p0 += 32) {
+        const unsigned tb = s_take[p0 >> 5];
+        const int at = pos + __popc(tb & lt_mask);
+        if (((tb >> lane) & 1u) && at < a.k_max) out[at] = p0 + lane;
+        pos += __popc(tb);
     }
     if (tid == 0) {
         if (total > a.k_max) raise_status(a.status, SPD_DEV_BAD_SEL);
@@ -773,7 +771,7 @@ cudaError_t launch_score_select(const ScoreSelectArgs& a, int num_sms, cudaStrea
     cudaError_t e = a.D == 128 ? launch_score_t<128>(a, grid, st) : launch_score_t<64>(a, grid, st);
     if (e != cudaSuccess) return e;
     // selection: one CTA per row, the row's keys in shared memory
-    const size_t smem = (size_t)a.max_pages * sizeof(uint32_t);
+    const size_t smem = ((size_t)a.max_pages + 2 * (((size_t)a.max_pages + 31) / 32)) * sizeof(uint32_t);
     e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(select_kernel, dim3((unsigned)((long long)a.B * a.H_kv)), dim3(kSelThreads), smem, st, a);
