@@ -111,6 +111,10 @@ __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Release / acquire fence at GPU scope (lighter than the sequentially consistent
+// __threadfence): followed by a relaxed write it forms a release pattern.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ bool flag_wait_bounded(const unsigned* flag, unsigned value, unsigned* status) {
     if (ld_acquire(flag) >= value) return true;
     const unsigned long long t0 = globaltimer_ns();

@@ -23,12 +23,14 @@
 // common order is exact), so no shuffles or ldmatrix are needed.
 //
 // Selection (a second kernel, one CTA per (sequence, KV head) row): the
-// mandatory pages, then the k'-th best score by an 8-bit radix select over
+// mandatory pages, then the k'-th best score by a radix select over
 // order-preserving uint32 keys (shared-memory histogram with warp-aggregated
-// atomics, since neighbouring scores share their high bytes).  As soon as the
-// digit being refined holds at most 256 keys (after two passes, typically),
-// those keys are ranked pairwise by (key desc, page asc) instead; otherwise the
-// four passes end on the exact k'-th key.  Pages above the boundary plus the
+// atomics, since neighbouring scores share bins).  The first digit is the 8
+// bits below those all candidates share (where their minimum and maximum
+// agree), so it already spreads them; as soon as the digit being refined holds
+// at most 256 keys (after one pass, typically) those keys are ranked pairwise
+// by (key desc, page asc) instead; otherwise the passes end on the exact k'-th
+// key.  Pages above the boundary plus the
 // boundary pages that rank (or, at an exact key, the lowest-id pages equal to
 // it) are compacted in ascending order into sel[] with ballots.
 #include "common.cuh"
@@ -224,6 +226,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
     extern __shared__ uint32_t keys[];
     __shared__ uint32_t hist[256];
     __shared__ int s_digit, s_rem, s_cnt, s_ncol;
+    __shared__ uint32_t s_kmin, s_kmax;
     __shared__ int w_eq[kSelWarps], w_take[kSelWarps];
     __shared__ uint32_t col_key[kRankMax];
     __shared__ int col_p[kRankMax];
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
     // chained step: the row's selection is published to the attention kernel
     auto publish = [&]() {
         if (!a.sel_done) return;
-        __threadfence();
+        fence_acq_rel_gpu();
         __syncthreads();
         if (tid == 0) st_release(a.sel_done + row, 1u);
     };
@@ -272,8 +275,15 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
     const int ncand = P - nm;
     auto mand = [&](int p) { return p < sink || p >= P - local; };
 
-    // keys: each thread's loads are independent and issued back to back
+    // keys: each thread's loads are independent and issued back to back; the
+    // candidates' smallest and largest key on the way
+    if (tid == 0) {
+        s_kmin = 0xffffffffu;
+        s_kmax = 0u;
+    }
+    __syncthreads();
     const float* sc = a.scores + (long long)row * a.max_pages;
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
     for (int p0 = 0; p0 < P; p0 += kSelThreads * 4) {
         float v[4];
 #pragma unroll
@@ -284,8 +294,21 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int p = p0 + i * kSelThreads + tid;
-            if (p < P) keys[p] = float_key(v[i]);
+            if (p < P) {
+                const uint32_t u = float_key(v[i]);
+                keys[p] = u;
+                if (!mand(p)) {
+                    kmin = min(kmin, u);
+                    kmax = max(kmax, u);
+                }
+            }
         }
+    }
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    if (lane == 0) {
+        atomicMin(&s_kmin, kmin);
+        atomicMax(&s_kmax, kmax);
     }
     __syncthreads();
 
@@ -312,7 +335,18 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
         rem = ncand;
     } else {
         rem = kp;
-        for (int shift = 24; shift >= 0; shift -= 8) {
+        // The bits above h are the same in every candidate (their minimum and maximum
+        // agree there): the radix starts below them, so the first digit already
+        // spreads the keys.  Digits of up to 8 bits until the boundary digit holds at
+        // most kRankMax keys (then ranked) or every bit is refined (an exact key).
+        int h = 31 - __clz((int)(s_kmin ^ s_kmax));  // -1 when all candidates are equal
+        pmask = h < 0 ? 0xffffffffu : (h >= 31 ? 0u : ~((2u << h) - 1u));
+        prefix = s_kmin & pmask;
+        int ncnt = ncand;
+        while (h >= 0 && ncnt > kRankMax) {
+            const int wd = h + 1 < 8 ? h + 1 : 8;
+            const int shift = h + 1 - wd;
+            const uint32_t dmask = (1u << wd) - 1u;
             hist[tid] = 0;  // kSelThreads == 256 bins
             __syncthreads();
             for (int p0 = 0; p0 < P; p0 += kSelThreads) {
@@ -322,7 +356,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
                 if (p < P && !mand(p)) {
                     const uint32_t u = keys[p];
                     in = (u & pmask) == prefix;
-                    bin = (u >> shift) & 255u;
+                    bin = (u >> shift) & dmask;
                 }
                 const unsigned act = __ballot_sync(0xffffffffu, in);
                 if (in) {  // neighbouring scores share bins: one atomic per distinct bin
@@ -332,7 +366,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
             }
             __syncthreads();
             if (warp == 0) {
-                // lane l owns bins 255-8l .. 248-8l, visited from the top
+                // lane l owns bins 255-8l .. 248-8l, visited from the top (bins past
+                // the digit's width stay empty)
                 uint32_t cnt[8];
                 int sum = 0;
 #pragma unroll
@@ -364,13 +399,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
             }
             __syncthreads();
             prefix |= (uint32_t)s_digit << shift;
-            pmask |= 255u << shift;
+            pmask |= dmask << shift;
             rem = s_rem;
-            if (shift > 0 && s_cnt <= kRankMax) {  // few enough: rank them (block-uniform)
-                ranked = true;
-                break;
-            }
+            ncnt = s_cnt;
+            h = shift - 1;
         }
+        ranked = ncnt <= kRankMax;  // block-uniform
         thr = prefix;
     }
     if (ranked) {
@@ -615,7 +649,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
     int pend_row = -1, pend_cnt = 0;  // tiles finished but not yet reported
     auto report = [&]() {
         if (pend_cnt == 0) return;
-        __threadfence();  // this warp's score (and append) stores before the count
+        fence_acq_rel_gpu();  // this warp's score (and append) stores before the count
         __syncwarp();
         if (lane == 0) atomicAdd(a.tiles_done + pend_row, (unsigned)pend_cnt);
         pend_cnt = 0;
@@ -745,7 +779,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
                 pend_row = row;
             }
             ++pend_cnt;
-            if ((g + 1) % kChunkTiles == 0 || g + 1 == total) report();  // end of a chunk
+            // end of a run of consecutive tiles (a chunk): the next tile in flight is not g + 1
+            if (gq[(slot + 1) % kScoreStages] != g + 1) report();
         }
         gq[slot] = grab(t + kScoreStages);
         if (gq[slot] >= 0) issue(t + kScoreStages, gq[slot]);

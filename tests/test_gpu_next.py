@@ -5,7 +5,7 @@ import pytest
 
 import oracle
 from sparse_attention_decode_pages_gb300 import workloads as wl
-from tests.gpu_helpers import Gpu, summ_bits
+from tests.gpu_helpers import Gpu, assert_close_outputs, compare_selection, np_bf16, summ_bits
 from tests.helpers import custom
 
 pytestmark = pytest.mark.gpu
@@ -311,20 +311,54 @@ def test_fused_append_flags_empty_sequences_and_bad_pages():
     assert g.sync_status() == 0x8 | 0x1
 
 
-# ---------------------------------------------------------------- the chained decode step
+# ---------------------------------------------------------------- the decode step in one call
 
-@pytest.mark.parametrize("name,kw,append", [
-    ("q8b", dict(), True),                                              # full size: chained rows
-    ("q8b", dict(B=5, len_lo=700, len_hi=2200), True),                  # few rows: calls in turn
-    ("q17b", dict(B=48, len_lo=2000, len_hi=6000), False),
-    ("longtail", dict(B=2, len_lo=4000, len_hi=9000, T=1), True)])
-def test_decode_step_equals_the_separate_calls(name, kw, append):
+def _top_p(w):
+    """The workload with a top-p budget (0.9 of the page weight) and room for every page."""
+    import dataclasses
+    import math
+    w.policy = dataclasses.replace(w.policy, mode="top_p", top_p=0.9, score_scale=1.0 / math.sqrt(w.D))
+    w.k_max = w.max_pages_per_seq
+    return w
+
+
+def _wide_table(w, max_pages=1040):
+    """The workload with a page table (and summary array) of max_pages slots per sequence."""
+    extra = max_pages - w.max_pages_per_seq
+    w.page_table = np.pad(w.page_table, ((0, 0), (0, extra)), constant_values=-1)
+    w.max_pages_per_seq = max_pages
+    return w
+
+
+# name, overrides, append, variant; "chained" cases have enough rows for one
+# attention unit per row, "calls" cases run the calls one after the other
+STEP_CASES = [
+    ("q8b", dict(), True, None),                                            # full size, chained
+    ("q8b", dict(B=5, len_lo=700, len_hi=2200), True, None),                # few rows: calls in turn
+    ("q17b", dict(B=48, len_lo=2000, len_hi=6000), False, None),            # chained
+    ("longtail", dict(B=2, len_lo=4000, len_hi=9000, T=1), True, None),     # calls
+    ("q8b", dict(B=40, len_lo=2000, len_hi=5000, page_size=32), True, None),
+    ("q8b", dict(B=40, len_lo=2000, len_hi=5000, page_size=64), False, None),
+    ("tiny", dict(B=200), True, None),                                      # D = 64, chained
+    ("q8b", dict(B=40, len_lo=2000, len_hi=5000), True, "top_p"),
+    ("q8b", dict(B=40, len_lo=2000, len_hi=5000), True, "wide_table"),
+]
+
+
+@pytest.mark.parametrize("name,kw,append,variant", STEP_CASES)
+def test_decode_step_equals_the_separate_calls(name, kw, append, variant):
     """sparse_decode_step gives the bits of append + score_select + sparse attention, for
     two steps in a row with different queries through one workspace (so the chain's
-    counters must have been reset by the first)."""
+    counters must have been reset by the first), chained row by row or as calls in turn,
+    at page sizes 16 / 32 / 64, head dims 64 / 128, top-p budgets and page tables
+    wider than the sequences."""
     import torch
     import sparse_attention_decode_pages_gb300 as spd
     w = wl.named(name, threads=8, **kw)
+    if variant == "top_p":
+        w = _top_p(w)
+    elif variant == "wide_table":
+        w = _wide_table(w)
     k_new, v_new = _new_tokens(w, 1, 31)
     rng = np.random.default_rng(32)
     q2 = torch.from_numpy(wl.f32_to_bf16_bits(rng.standard_normal(w.q.shape).astype(np.float32))).view(
@@ -362,3 +396,87 @@ def test_decode_step_equals_the_separate_calls(name, kw, append):
     names = ["K", "summ", "sel", "nsel", "o", "lse"] * 2
     for x, y, what in zip(outs[0], outs[1], names):
         assert np.array_equal(x, y), what
+
+
+def _edge_lens(n_seq, ps):
+    """Lengths cycling through the edge cases: empty, one token, a page minus one, a
+    page, a page plus one, and longer ragged rows."""
+    pattern = [0, 1, ps - 1, ps, ps + 1, 2 * ps + 1, 100, 20 * ps + 3]
+    return [pattern[i % len(pattern)] for i in range(n_seq)]
+
+
+@pytest.mark.parametrize("case", ["q17b_short", "tiny_d64", "edges_d128", "edges_d64_ps32"])
+def test_decode_step_against_the_oracle(case):
+    """The chained decode step (no append; enough rows for one attention unit per row)
+    against the fp64 oracle: selections equal outside the tie band, outputs within
+    tolerance on the rows selected alike, empty rows give o = 0 and lse = -inf."""
+    import torch
+    import sparse_attention_decode_pages_gb300 as spd
+    if case == "q17b_short":
+        w = wl.named("q17b", threads=8, B=40, len_lo=300, len_hi=1500,
+                     policy=wl.BudgetPolicy("fixed", fixed_pages=24, sink_pages=1, local_pages=4))
+    elif case == "tiny_d64":
+        w = wl.named("tiny", threads=8, B=200)
+    else:
+        D, ps = (128, 16) if case == "edges_d128" else (64, 32)
+        pol = wl.BudgetPolicy("fixed", fixed_pages=3, sink_pages=1, local_pages=1)
+        w = custom(_edge_lens(200, ps), 4, 2, D, ps, rng=np.random.default_rng(D + ps), policy=pol, k_max=8)
+    ref = oracle.decode_step(w, threads=8)
+    g = Gpu(w)
+    summ = g.summarize()
+    d = g.d
+    sel = torch.full((w.B, w.H_kv, w.k_max), -1, dtype=torch.int32, device="cuda")
+    nsel = torch.full((w.B, w.H_kv), -7, dtype=torch.int32, device="cuda")
+    o = torch.full((w.B, w.H_q, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((w.B, w.H_q), float("nan"), device="cuda")
+    ws = g.ws(spd.spd_sparse_decode_step_workspace_size(g.dims, w.k_max))
+    spd.sparse_decode_step(g.dims, d["K"], d["V"], d["page_table"], d["seq_lens"], None, None, d["q"], summ,
+                           w.policy, sel, nsel, w.k_max, o, ws, lse=lse)
+    assert g.sync_status() == 0
+    _, _, sc, _ = g.score_select(summ)   # the GPU's own scores, for the validity check
+    same = compare_selection(w, sel.cpu().numpy(), nsel.cpu().numpy(), sc.cpu().numpy(), ref["sel"], ref["nsel"],
+                             ref["scores"])
+    seqs_same = sorted({b for b, h in same if all((b, hh) in same for hh in range(w.H_kv))})
+    assert len(seqs_same) >= w.B // 2
+    assert_close_outputs(np_bf16(o)[seqs_same], ref["o"][seqs_same], lse.cpu().numpy()[seqs_same],
+                         ref["lse"][seqs_same], what=f"decode step {case}")
+    empty = [b for b in range(w.B) if int(w.seq_lens[b]) == 0]
+    if empty:
+        assert not np_bf16(o)[empty].any()
+        assert np.all(np.isneginf(lse.cpu().numpy()[empty]))
+        assert not nsel.cpu().numpy()[empty].any()
+
+
+def test_decode_step_ties_go_to_lower_pages():
+    """Pages with identical keys score alike: the chained step takes the mandatory pages
+    and then the lowest page ids, at 41 and at 100 pages per row."""
+    import torch
+    import sparse_attention_decode_pages_gb300 as spd
+    ps, D, H_kv = 16, 64, 2
+    lens = [16 * 40 + 5 if i % 2 == 0 else 16 * 99 + 1 for i in range(200)]
+    rng = np.random.default_rng(77)
+    K = []
+    for n in lens:
+        tok = rng.standard_normal((1, H_kv, D)).astype(np.float32)
+        K.append(np.repeat(tok, n, axis=0))
+    pol = wl.BudgetPolicy("fixed", fixed_pages=8, sink_pages=1, local_pages=1)
+    w = custom(lens, 4, H_kv, D, ps, rng=rng, K=K, policy=pol, k_max=8)
+    g = Gpu(w)
+    summ = g.summarize()
+    d = g.d
+    sel = torch.full((w.B, w.H_kv, w.k_max), -1, dtype=torch.int32, device="cuda")
+    nsel = torch.full((w.B, w.H_kv), -7, dtype=torch.int32, device="cuda")
+    o = torch.empty((w.B, w.H_q, w.D), dtype=torch.bfloat16, device="cuda")
+    ws = g.ws(spd.spd_sparse_decode_step_workspace_size(g.dims, w.k_max))
+    spd.sparse_decode_step(g.dims, d["K"], d["V"], d["page_table"], d["seq_lens"], None, None, d["q"], summ,
+                           w.policy, sel, nsel, w.k_max, o, ws)
+    assert g.sync_status() == 0
+    sel_h, nsel_h = sel.cpu().numpy(), nsel.cpu().numpy()
+    ref = oracle.decode_step(w, threads=8)
+    for b in range(w.B):
+        P = w.pages(b)
+        expect = [0, 1, 2, 3, 4, 5, 6, P - 1]
+        for h in range(H_kv):
+            assert nsel_h[b, h] == 8
+            assert sel_h[b, h].tolist() == expect, (b, h, sel_h[b, h].tolist())
+            assert ref["sel"][b, h, :8].tolist() == expect
