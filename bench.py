@@ -19,8 +19,8 @@ kernel is timed with CUDA events on the launching stream; L2 is evicted between 
 dirty lines to be written back during the next timed kernel).  The KV cache and the
 page summaries are resident in HBM (they are the cache); e2e adds, per step,
 the host->device copy of the step's inputs (q, the new token's K / V,
-seq_lens, page_table) from
-pinned memory and the device->host copy of o and lse.
+seq_lens, page_table), staged in one pinned buffer, to the
+device and the copy of o and lse back, one copy each way.
 
 --impl reference times the fp64 CPU oracle (there is no other reference
 implementation of this path) on the same workload and metric.
@@ -58,6 +58,23 @@ def kernel_source_hash() -> str:
         with open(os.path.join(ROOT, "sparse_attention_decode_pages_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def staged(torch, dev, tensors):
+    """One device buffer holding the given tensors back to back (each at a 256-byte
+    aligned offset), and views of it with their shapes, dtypes and values: a step's
+    inputs (or outputs) then move between host and device in one copy."""
+    offs, total = [], 0
+    for t in tensors:
+        offs.append(total)
+        total += -(-t.numel() * t.element_size() // 256) * 256
+    buf = torch.empty(total, dtype=torch.uint8, device=dev)
+    views = []
+    for t, off in zip(tensors, offs):
+        v = buf[off:off + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        views.append(v)
+    return buf, views
 
 
 def replica_seed(base_seed: int, rank: int) -> int:
@@ -217,6 +234,10 @@ def run_gpu(args):
     nsel = torch.empty((w.B, w.H_kv), dtype=torch.int32, device=dev)
     o = torch.empty((w.B, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.H_q), dtype=torch.float32, device=dev)
+    # the step's inputs and outputs each in one device buffer (one copy each way in e2e)
+    inp_d, (d["q"], d["seq_lens"], d["page_table"], k_new, v_new) = staged(
+        torch, dev, [d["q"], d["seq_lens"], d["page_table"], k_new, v_new])
+    out_d, (o, lse) = staged(torch, dev, [o, lse])
     ov = torch.empty((w.B, T, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
     lsev = torch.empty((w.B, T, w.H_q), dtype=torch.float32, device=dev)
     ws_sel = spd.workspace(spd.spd_score_select_workspace_size(dims), dev)
@@ -323,33 +344,25 @@ def run_gpu(args):
     ms_ver = float(np.mean(t_ver))
     ms_att = float(np.mean(t_att))
 
-    # e2e: the same sparse pass through the C ABI with host buffers.
-    q_h = d["q"].cpu().pin_memory()
-    sl_h = d["seq_lens"].cpu().pin_memory()
-    pt_h = d["page_table"].cpu().pin_memory()
-    kn_h = k_new.cpu().pin_memory()
-    vn_h = v_new.cpu().pin_memory()
-    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    # e2e: the same sparse pass through the C ABI with host buffers: the step's inputs
+    # (q, seq_lens, page_table, the new token's K / V) staged in one pinned buffer and
+    # copied in, o and lse copied out.
+    inp_h = inp_d.cpu().pin_memory()
+    out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
     e2e_ms = []
     for i in range(args.warmup + args.steps):
         flush.zero_()
         ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ea.record(stream)
-        d["q"].copy_(q_h, non_blocking=True)
-        d["seq_lens"].copy_(sl_h, non_blocking=True)
-        d["page_table"].copy_(pt_h, non_blocking=True)
-        k_new.copy_(kn_h, non_blocking=True)
-        v_new.copy_(vn_h, non_blocking=True)
+        inp_d.copy_(inp_h, non_blocking=True)
         sparse_pass()
-        o_h.copy_(o, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        out_h.copy_(out_d, non_blocking=True)
         eb.record(stream)
         eb.synchronize()
         if i >= args.warmup:
             e2e_ms.append(ea.elapsed_time(eb))
-    h2d = q_h.numel() * 2 + sl_h.numel() * 4 + pt_h.numel() * 4 + (kn_h.numel() + vn_h.numel()) * 2
-    d2h = o_h.numel() * 2 + lse_h.numel() * 4
+    h2d = inp_h.numel()  # bytes, with each input padded to 256
+    d2h = out_h.numel()
 
     nxt = None if args.no_next else next_rows(spd, torch, w, d, dims, summ, stream, flush, peak_of=hbm_peak,
                                               reps=max(10, min(args.steps, 50)), warmup=args.warmup)
