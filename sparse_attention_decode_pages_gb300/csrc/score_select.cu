@@ -93,11 +93,14 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
 // Query-dependent budget: the number of non-mandatory pages that, taken in
 // score order after the mandatory ones, bring the selected page weight to
 // top_p of the total (all of them if none does).  Weights are integers on a
-// 2^-31 grid, so every sum is exact.  The k'-th page is found by an 8-bit radix
-// descent over the keys in which each bin carries its count and its weight.
+// 2^-31 grid, so every sum is exact; each page's weight is computed once (into
+// wts).  The k'-th page is found by a radix descent over the keys in which each
+// bin carries its count and its weight, starting below the bits all candidates
+// share (kmin / kmax: their smallest and largest key).
 template <class Mand>
 __device__ int top_p_pages(const ScoreSelectArgs& a, const uint32_t* keys, int P, Mand mand,
-                           uint32_t* hist, int& s_digit, int& s_rem) {
+                           uint32_t* hist, int& s_digit, int& s_rem, uint32_t kmin, uint32_t kmax,
+                           uint32_t* wts) {
     typedef unsigned long long u64;
     __shared__ u64 mhist[256];
     __shared__ u64 red[kSelWarps];
@@ -117,7 +120,8 @@ __device__ int top_p_pages(const ScoreSelectArgs& a, const uint32_t* keys, int P
     const float c2 = a.pol.score_scale * 1.4426950408889634f;
     u64 tot = 0, man = 0;
     for (int p = tid; p < P; p += kSelThreads) {
-        const u64 w = page_weight(keys[p], smax, c2);
+        const uint32_t w = page_weight(keys[p], smax, c2);
+        wts[p] = w;
         tot += w;
         if (mand(p)) man += w;
     }
@@ -128,11 +132,17 @@ __device__ int top_p_pages(const ScoreSelectArgs& a, const uint32_t* keys, int P
     if (need <= held) return 0;
     u64 R = need - held;
 
-    uint32_t prefix = 0, pmask = 0;
-    u64 above = 0;   // weight of the candidates above the current prefix
-    int n_above = 0; // and their count
-    int eq_count = 0;
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    // bits above h are the same in every candidate
+    int h = 31 - __clz((int)(kmin ^ kmax));  // -1 when all candidates are equal
+    uint32_t pmask = h < 0 ? 0xffffffffu : (h >= 31 ? 0u : ~((2u << h) - 1u));
+    uint32_t prefix = kmin & pmask;
+    u64 above = 0;        // weight of the candidates above the current prefix
+    int n_above = 0;      // and their count
+    int eq_count = ncand; // candidates matching the prefix
+    while (h >= 0) {
+        const int wd = h + 1 < 8 ? h + 1 : 8;
+        const int shift = h + 1 - wd;
+        const uint32_t dmask = (1u << wd) - 1u;
         hist[tid] = 0;
         mhist[tid] = 0;
         __syncthreads();
@@ -144,8 +154,8 @@ __device__ int top_p_pages(const ScoreSelectArgs& a, const uint32_t* keys, int P
                 const uint32_t u = keys[p];
                 if ((u & pmask) == prefix) {
                     in = true;
-                    bin = (u >> shift) & 255u;
-                    w = page_weight(u, smax, c2);
+                    bin = (u >> shift) & dmask;
+                    w = wts[p];
                 }
             }
             // neighbouring scores share bins: one pair of atomics per distinct bin in the
@@ -211,7 +221,8 @@ __device__ int top_p_pages(const ScoreSelectArgs& a, const uint32_t* keys, int P
         n_above += s_rem;
         eq_count = (int)hist[s_digit];
         prefix |= (uint32_t)s_digit << shift;
-        pmask |= 255u << shift;
+        pmask |= dmask << shift;
+        h = shift - 1;
         __syncthreads();  // hist / s_* are rewritten by the next level
     }
     // every candidate whose key equals prefix has the same weight
@@ -314,7 +325,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
 
     long long k;
     if (a.pol.mode == SPD_BUDGET_TOP_P)
-        k = nm + top_p_pages(a, keys, P, mand, hist, s_digit, s_rem);
+        k = nm + top_p_pages(a, keys, P, mand, hist, s_digit, s_rem, s_kmin, s_kmax,
+                             s_take + (a.max_pages + 31) / 32);
     else
         k = budget_pages(a.pol, len, a.ps);
     if (k > a.k_max) k = a.k_max;
@@ -806,7 +818,9 @@ cudaError_t launch_score_select(const ScoreSelectArgs& a, int num_sms, cudaStrea
     cudaError_t e = a.D == 128 ? launch_score_t<128>(a, grid, st) : launch_score_t<64>(a, grid, st);
     if (e != cudaSuccess) return e;
     // selection: one CTA per row, the row's keys in shared memory
-    const size_t smem = ((size_t)a.max_pages + 2 * (((size_t)a.max_pages + 31) / 32)) * sizeof(uint32_t);
+    // keys, chosen and decision bit words, and (top-p) the page weights
+    const size_t smem = ((size_t)a.max_pages + 2 * (((size_t)a.max_pages + 31) / 32) +
+                         (a.pol.mode == SPD_BUDGET_TOP_P ? (size_t)a.max_pages : 0)) * sizeof(uint32_t);
     e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(select_kernel, dim3((unsigned)((long long)a.B * a.H_kv)), dim3(kSelThreads), smem, st, a);
