@@ -232,26 +232,48 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
             // Items are issued in multiples of KS (padding items carry no page), so
             // every unit starts on group 0 and each group sees each unit.
             const int cpad = (count + KS - 1) / KS * KS;
+            // Items are resolved 32 at a time (lane i: item base + i).  The first batch's
+            // page-table entries are read here; each later batch's selection entries and
+            // page-table entries are read while the batch before it is being issued, so
+            // the ring does not drain between batches.
+            int lp_raw = -1;         // this lane's logical page in the current batch (unchecked)
+            long long ph_raw = -1;   // and its page-table entry (read when lp_raw is in range)
+            if (lane < count) {
+                lp_raw = SPARSE ? pre : start + lane;
+                if (lp_raw >= 0 && lp_raw < P) ph_raw = a.page_table[(long long)b * a.max_pages + lp_raw];
+            }
             for (int base = 0; base < cpad && ok; base += 32) {
-                // resolve 32 items in one round trip
                 int lp = -1;
                 long long phys = -1;
                 if (base + lane < count) {
-                    const int it = start + base + lane;
-                    lp = SPARSE ? (base == 0 ? pre : a.sel[(long long)row * a.k_max + it]) : it;
+                    lp = lp_raw;
                     if (lp < 0 || lp >= P) {
                         raise_status(a.status, SPD_DEV_BAD_SEL);
                         lp = -1;
                     } else {
-                        phys = a.page_table[(long long)b * a.max_pages + lp];
+                        phys = ph_raw;
                         if (phys < 0 || phys >= a.num_phys) {
                             raise_status(a.status, SPD_DEV_BAD_PAGE);
                             lp = -1;
                         }
                     }
                 }
+                // the next batch: its logical pages now, its page-table entries after a
+                // few of this batch's pages are issued (by then the pages have arrived)
+                const int nbase = base + 32;
+                int lp_next = -1;
+                long long ph_next = -1;
+                bool ph_read = false;
+                if (nbase + lane < count)
+                    lp_next = SPARSE ? a.sel[(long long)row * a.k_max + start + nbase + lane] : start + nbase + lane;
+                auto read_next_page_table = [&]() {
+                    if (nbase + lane < count && lp_next >= 0 && lp_next < P)
+                        ph_next = a.page_table[(long long)b * a.max_pages + lp_next];
+                    ph_read = true;
+                };
                 const int nb = min(32, cpad - base);
                 for (int k = 0; k < nb; ++k) {
+                    if (k == 4 && nbase < count) read_next_page_table();
                     const int lpk = __shfl_sync(0xffffffffu, lp, k);
                     const long long pk = __shfl_sync(0xffffffffu, phys, k);
                     if (!slot_free(j)) {
@@ -285,6 +307,9 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
                     }
                     ++j;
                 }
+                if (!ph_read && nbase < count) read_next_page_table();
+                lp_raw = lp_next;
+                ph_raw = ph_next;
             }
             ++seq;
         }
