@@ -411,9 +411,14 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
             const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
 #pragma unroll
             for (int cc = 0; cc < PS / 16; ++cc) {
-                float s[2][4];
+                // S = Q K^T: even and odd k-steps accumulate in separate chains (four
+                // independent MMA chains instead of two), added at the end
+                float s[2][4], s_odd[2][4];
 #pragma unroll
-                for (int i = 0; i < 2; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+                for (int i = 0; i < 2; ++i) {
+                    s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+                    s_odd[i][0] = s_odd[i][1] = s_odd[i][2] = s_odd[i][3] = 0.f;
+                }
                 {
                     const int mi = lane >> 3, rr = lane & 7;
                     const int tok = cc * 16 + (mi >> 1) * 8 + rr;
@@ -423,9 +428,14 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
                         const uint32_t addr = kbase + (chunk >> 3) * HALF_BYTES + swz128(tok, chunk & 7);
                         uint32_t b0, b1, b2, b3;
                         ldsm_x4(addr, b0, b1, b2, b3);
-                        mma_bf16(s[0], qa[kk], b0, b1);
-                        mma_bf16(s[1], qa[kk], b2, b3);
+                        float(*acc)[4] = (kk & 1) ? s_odd : s;
+                        mma_bf16(acc[0], qa[kk], b0, b1);
+                        mma_bf16(acc[1], qa[kk], b2, b3);
                     }
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) s[i][e] += s_odd[i][e];
                 }
                 const int tok0 = page_start + cc * 16;
                 const bool need_mask = tok0 + 15 > lim_min;
