@@ -633,15 +633,26 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
     // Chained step: chunks of kChunkTiles consecutive tiles are taken from the counter
     // (rows finish in order), and a warp reports finished tiles to their row once
     // per chunk (or row change), behind one fence.
-    bool drained = false;
+    bool drained = false, first_chunk = true;
     long long ch_cur = 0, ch_end = 0;
     auto grab = [&](int t) -> long long {
         if (!a.tile_ctr) return g0 + t < g1 ? g0 + t : -1;
         if (ch_cur < ch_end) return ch_cur++;
         if (drained) return -1;
+        if (first_chunk) {
+            // warp gw's first chunk is chunk gw (no round trip before the first copy);
+            // the counter hands out the chunks after the first nwarps
+            first_chunk = false;
+            const long long v0 = gw * kChunkTiles;
+            if (v0 < total) {
+                ch_cur = v0 + 1;
+                ch_end = min(v0 + kChunkTiles, total);
+                return v0;
+            }
+        }
         unsigned long long v = 0;
         if (lane == 0) {
-            v = atomicAdd(a.tile_ctr, (unsigned long long)kChunkTiles);
+            v = atomicAdd(a.tile_ctr, (unsigned long long)kChunkTiles) + (unsigned long long)(nwarps * kChunkTiles);
             if ((long long)v >= total) {  // each warp fails exactly once; the last one resets
                 if (atomicAdd(a.warps_done, 1u) == (unsigned)nwarps - 1) {
                     *a.tile_ctr = 0ull;
