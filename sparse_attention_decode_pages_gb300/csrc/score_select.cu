@@ -22,7 +22,8 @@
 // the query operand uses the same order (the contraction is a sum, so any
 // common order is exact), so no shuffles or ldmatrix are needed.
 //
-// Selection (a second kernel, one CTA per (sequence, KV head) row): the
+// Selection (a second kernel; a CTA per (sequence, KV head) row, or in the
+// chained step two persistent CTAs per SM taking the rows in order): the
 // mandatory pages, then the k'-th best score by a radix select over
 // order-preserving uint32 keys (shared-memory histogram with warp-aggregated
 // atomics, since neighbouring scores share bins).  The first digit is the 8
@@ -231,10 +232,9 @@ __device__ int top_p_pages(const ScoreSelectArgs& a, const uint32_t* keys, int P
     return n_above + (int)min((u64)eq_count, t);
 }
 
-// Selection of one (sequence, KV head) row by a CTA of 8 warps.  keys holds
-// the row's order-preserving score keys in shared memory.
-__global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) {
-    extern __shared__ uint32_t keys[];
+// Selection of one (sequence, KV head) row by a CTA of 8 warps.  keys: the
+// dynamic shared memory (the row's order-preserving score keys, then bit words).
+__device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const int row, uint32_t* keys) {
     __shared__ uint32_t hist[256];
     __shared__ int s_digit, s_rem, s_cnt, s_ncol;
     __shared__ uint32_t s_kmin, s_kmax;
@@ -246,12 +246,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
     uint32_t* s_take = s_chosen + (a.max_pages + 31) / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned lt_mask = (1u << lane) - 1u;
-    const int row = blockIdx.x;
     const int b = row / a.H_kv;
     __shared__ int s_ok;
     if (a.tiles_done) {
         // chained step: wait for this row's tiles only, not for the whole scoring grid
-        pdl_trigger();
         if (tid == 0) {
             const int P0 = (a.seq_lens[b] + a.ps - 1) / a.ps;
             s_ok = flag_wait_bounded(a.tiles_done + row, (unsigned)((P0 + 15) / 16), a.status);
@@ -259,9 +257,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
         }
         __syncthreads();
         if (!s_ok) return;
-    } else {
-        pdl_wait();
-        pdl_trigger();
     }
     // chained step: the row's selection is published to the attention kernel
     auto publish = [&]() {
@@ -509,6 +504,25 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
         a.nsel[row] = min(total, a.k_max);
     }
     publish();
+}
+
+// One CTA per row, or (chained step) two CTAs per SM, each selecting rows
+// blockIdx.x, blockIdx.x + gridDim.x, ... in order: they are all resident beside
+// the scoring CTAs from the start, so the attention grid, which launches once every
+// selection CTA has started, is launched early.
+__global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) {
+    extern __shared__ uint32_t keys[];
+    if (a.tiles_done) {
+        pdl_trigger();  // each row waits for its own tiles instead of the scoring grid
+    } else {
+        pdl_wait();
+        pdl_trigger();
+    }
+    const int rows = a.B * a.H_kv;
+    for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+        select_row_block(a, row, keys);
+        __syncthreads();  // the shared state is reused by the next row
+    }
 }
 
 // Fused append of the step's token for row (b, h): the token at position
@@ -834,7 +848,9 @@ cudaError_t launch_score_select(const ScoreSelectArgs& a, int num_sms, cudaStrea
                          (a.pol.mode == SPD_BUDGET_TOP_P ? (size_t)a.max_pages : 0)) * sizeof(uint32_t);
     e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(select_kernel, dim3((unsigned)((long long)a.B * a.H_kv)), dim3(kSelThreads), smem, st, a);
+    long long sgrid = (long long)a.B * a.H_kv;
+    if (a.tiles_done && sgrid > 2LL * num_sms) sgrid = 2LL * num_sms;
+    return launch_pdl(select_kernel, dim3((unsigned)sgrid), dim3(kSelThreads), smem, st, a);
 }
 
 }  // namespace spd
