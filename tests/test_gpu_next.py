@@ -268,7 +268,7 @@ def test_fused_append_score_select_equals_the_two_calls(name, kw):
     w = wl.named(name, threads=4, **kw)
     k_new, v_new = _new_tokens(w, 1, 21)
     outs = []
-    for fused in (False, True):
+    for one_call in (False, True):
         g = Gpu(w)
         summ = g.summarize()
         kn = torch.from_numpy(k_new).view(torch.bfloat16).cuda()
@@ -278,7 +278,7 @@ def test_fused_append_score_select_equals_the_two_calls(name, kw):
         sc = torch.full((w.B, w.H_kv, w.max_pages_per_seq), float("nan"), device="cuda")
         ws = g.ws(spd.spd_score_select_workspace_size(g.dims))
         d = g.d
-        if fused:
+        if one_call:
             spd.pages_append_score_select(g.dims, d["K"], d["V"], d["page_table"], d["seq_lens"], kn, vn,
                                           d["q"], summ, w.policy, sel, nsel, w.k_max, ws, scores=sc)
         else:
@@ -364,7 +364,7 @@ def test_decode_step_equals_the_separate_calls(name, kw, append, variant):
     q2 = torch.from_numpy(wl.f32_to_bf16_bits(rng.standard_normal(w.q.shape).astype(np.float32))).view(
         torch.bfloat16).cuda()
     outs = []
-    for fused in (False, True):
+    for one_call in (False, True):
         g = Gpu(w)
         summ = g.summarize()
         d = g.d
@@ -379,7 +379,7 @@ def test_decode_step_equals_the_separate_calls(name, kw, append, variant):
         wsa = g.ws(spd.spd_sparse_decode_workspace_size(g.dims, w.k_max, 0))
         res = []
         for q in (d["q"], q2):
-            if fused:
+            if one_call:
                 spd.sparse_decode_step(g.dims, d["K"], d["V"], d["page_table"], d["seq_lens"], kn, vn, q,
                                        summ, w.policy, sel, nsel, w.k_max, o, ws, lse=lse)
             else:
