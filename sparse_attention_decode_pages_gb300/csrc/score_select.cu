@@ -692,7 +692,9 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
         pend_cnt = 0;
     };
 
-    // tile index -> (sequence, KV head, first page); shared-memory lookups only
+    // tile index -> (sequence, KV head, first page); shared-memory lookups only.  A
+    // row's tiles are numbered from its last page down, so the tile with the step's
+    // appended token comes first and its extra work does not delay the row's end.
     auto locate = [&](long long g, int& b, int& h, int& p0, int& P) {
         int lo = 0, hi = a.B - 1;
         while (lo < hi) {
@@ -705,7 +707,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
         const int tb = (P + 15) / 16;
         const int local = (int)(g - pref[b]);
         h = local / tb;
-        p0 = (local - h * tb) * 16;
+        p0 = (tb - 1 - (local - h * tb)) * 16;
     };
     int issued_row = -1;
     auto issue = [&](int t, long long g) {
