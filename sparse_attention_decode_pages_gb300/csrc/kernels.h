@@ -82,7 +82,6 @@ struct ScoreSelectArgs {
     int32_t* nsel;
     int k_max;
     float* scores;    // [B][H_kv][max_pages]
-    int* counters;    // [B][H_kv], zero on entry and on exit
     int B, H_q, H_kv, D, ps, max_pages;
     long long num_phys;
     unsigned* status;

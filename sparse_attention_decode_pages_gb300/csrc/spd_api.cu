@@ -230,7 +230,7 @@ SPD_API spd_status spd_device_status(uint32_t* out, int32_t clear) {
 SPD_API size_t spd_score_select_workspace_size(const spd_dims* dims) {
     if (check_dims(dims) != SPD_OK) return 0;
     const long long rows = (long long)dims->B * dims->H_kv;
-    return align256(rows * sizeof(int)) + (size_t)rows * dims->max_pages_per_seq * sizeof(float);
+    return align256((size_t)rows * dims->max_pages_per_seq * sizeof(float));  // the scores
 }
 
 SPD_API size_t spd_sparse_decode_workspace_size(const spd_dims* dims, int32_t k_max, int32_t num_splits) {
@@ -384,7 +384,6 @@ static spd_status score_select_setup(const spd_dims* dims, const spd_bf16* q, co
     if (!aligned16(ws)) return fail(SPD_ERR_INVALID_ARG, "ws must be 16-byte aligned");
     DevInfo* d = dev_info(&st);
     if (!d) return st;
-    const long long rows = (long long)dims->B * dims->H_kv;
     a = ScoreSelectArgs{};
     a.q = q;
     a.summ = summ;
@@ -393,8 +392,7 @@ static spd_status score_select_setup(const spd_dims* dims, const spd_bf16* q, co
     a.sel = sel;
     a.nsel = nsel;
     a.k_max = k_max;
-    a.counters = static_cast<int*>(ws);
-    a.scores = scores ? scores : reinterpret_cast<float*>(static_cast<char*>(ws) + align256(rows * sizeof(int)));
+    a.scores = scores ? scores : static_cast<float*>(ws);
     a.B = dims->B;
     a.H_q = dims->H_q;
     a.H_kv = dims->H_kv;

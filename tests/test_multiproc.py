@@ -71,3 +71,21 @@ def test_reference_arm_line_on_rank_zero():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["higher_is_better"] is True
+
+
+def test_staged_inputs_are_views_of_one_buffer():
+    """The benchmark's e2e copies a step's inputs in one transfer: staged() packs the
+    tensors at 256-byte offsets of one buffer, as views with their shapes, dtypes and
+    values."""
+    import torch
+    import bench
+    ts = [torch.arange(10, dtype=torch.int32), torch.randn(3, 5).to(torch.bfloat16),
+          torch.ones(70, dtype=torch.float32), torch.arange(6, dtype=torch.int32).reshape(2, 3)]
+    buf, views = bench.staged(torch, "cpu", ts)
+    assert buf.dtype == torch.uint8 and buf.numel() == 256 + 256 + 512 + 256
+    base = buf.data_ptr()
+    for t, v in zip(ts, views):
+        assert v.dtype == t.dtype and v.shape == t.shape and torch.equal(v, t)
+        assert (v.data_ptr() - base) % 256 == 0
+    views[0].fill_(7)  # a view: writes land in the buffer
+    assert torch.equal(buf[:40].view(torch.int32), torch.full((10,), 7, dtype=torch.int32))
