@@ -36,11 +36,12 @@
  *    log-sum-exp of the scaled logits.  A row that sees no token gets o = 0,
  *    lse = -inf.
  *  - Workspace: `ws` is caller-owned device scratch of at least the size the
- *    matching *_workspace_size function returns.  Its first bytes hold
- *    counters that MUST be zero before the first call that uses this buffer;
- *    every successful call leaves them zero again, so a buffer can be reused
- *    by any later call on the same stream.  Calls that overlap on the GPU must
- *    use different workspaces.
+ *    matching *_workspace_size function returns.  The counters and flags some
+ *    calls keep in it (unit queue, split tickets, the step's chain) MUST be
+ *    zero before the first call that uses the buffer (zero the whole buffer
+ *    once); every successful call leaves them zero again, so a buffer can be
+ *    reused by any later call on the same stream.  Calls that overlap on the
+ *    GPU must use different workspaces.
  *  - Errors: argument problems are reported synchronously by the returned
  *    status (nothing is launched); spd_last_error() gives a message.  Problems
  *    only the GPU can see (a page id outside [0, num_phys_pages), a selection
