@@ -73,7 +73,9 @@ typedef enum {
 #define SPD_DEV_BAD_PAGE 0x1u  /* a page-table entry outside [0, num_phys_pages) */
 #define SPD_DEV_BAD_SEL 0x2u   /* a selected page id outside the sequence, or nsel > k_max */
 #define SPD_DEV_TIMEOUT 0x4u   /* a bounded wait on an asynchronous copy ran out */
-#define SPD_DEV_BAD_LEN 0x8u   /* kv_append_refresh: seq_lens[b] < T or beyond the page table */
+#define SPD_DEV_BAD_LEN 0x8u   /* seq_lens[b] outside [0, max_pages_per_seq * page_size] (the row is
+                                * then treated as empty: nothing selected, o = 0, lse = -inf), or
+                                * too short for the tokens being appended */
 #define SPD_DEV_BAD_TOKEN 0x10u /* spec_accept: a drafted token outside [0, n_vocab) */
 
 /*

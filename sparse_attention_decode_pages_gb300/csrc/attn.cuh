@@ -188,7 +188,11 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
             int pre = -1;
             if (SPARSE && start + lane < a.k_max) pre = a.sel[(long long)row * a.k_max + start + lane];
             const int len = a.seq_lens[b];
-            const int P = (len + PS - 1) / PS;
+            int P = seq_pages(len, PS, a.max_pages);
+            if (P < 0) {  // a length the page table cannot hold: the row is empty
+                if (lane == 0) raise_status(a.status, SPD_DEV_BAD_LEN);
+                P = 0;
+            }
             int n_items;
             if (SPARSE) {
                 n_items = a.nsel[row];

@@ -205,6 +205,14 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
     return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// Pages of a sequence of len tokens, or -1 when len is outside [0, max_pages * ps]
+// (the page table has no room for it: the row is then treated as empty and
+// SPD_DEV_BAD_LEN raised by the caller).
+__device__ __forceinline__ int seq_pages(int len, int ps, int max_pages) {
+    if (len < 0 || (long long)len > (long long)max_pages * ps) return -1;
+    return (len + ps - 1) / ps;
+}
+
 // Order-preserving map of fp32 to uint32 (larger float -> larger key).
 __device__ __forceinline__ uint32_t float_key(float f) {
     uint32_t u = __float_as_uint(f);

@@ -251,7 +251,7 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
     if (a.tiles_done) {
         // chained step: wait for this row's tiles only, not for the whole scoring grid
         if (tid == 0) {
-            const int P0 = (a.seq_lens[b] + a.ps - 1) / a.ps;
+            const int P0 = max(0, seq_pages(a.seq_lens[b], a.ps, a.max_pages));  // as the scoring kernel counts
             s_ok = flag_wait_bounded(a.tiles_done + row, (unsigned)((P0 + 15) / 16), a.status);
             if (s_ok) a.tiles_done[row] = 0u;  // this row's count is consumed
         }
@@ -266,7 +266,7 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
         if (tid == 0) st_release(a.sel_done + row, 1u);
     };
     const int len = a.seq_lens[b];
-    const int P = (len + a.ps - 1) / a.ps;
+    const int P = max(0, seq_pages(len, a.ps, a.max_pages));  // a bad length: empty (flagged by the scoring)
     int32_t* out = a.sel + (long long)row * a.k_max;
     if (P <= 0) {
         if (tid == 0) {
@@ -618,7 +618,11 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
     pdl_trigger();
     // pref[b] = H_kv * (16-page tiles of sequences 0..b-1); a sequence's tiles are
     // ordered (KV head, tile).
-    for (int bb = threadIdx.x; bb < a.B; bb += kScoreThreads) pages[bb] = (a.seq_lens[bb] + a.ps - 1) / a.ps;
+    for (int bb = threadIdx.x; bb < a.B; bb += kScoreThreads) {
+        const int P = seq_pages(a.seq_lens[bb], a.ps, a.max_pages);
+        if (P < 0 && blockIdx.x == 0) raise_status(a.status, SPD_DEV_BAD_LEN);
+        pages[bb] = P < 0 ? 0 : P;  // a length the page table cannot hold: nothing to score
+    }
     __syncthreads();
     if (warp == 0) {
         int run = 0;

@@ -176,6 +176,42 @@ def test_bad_page_id_sets_status_and_does_not_fault():
     assert g.sync_status() == 0  # cleared
 
 
+@pytest.mark.parametrize("bad", ["long", "negative"])
+def test_length_beyond_the_page_table_sets_status_and_empties_the_row(bad):
+    """A seq_lens entry the page table cannot hold (longer than max_pages * page_size,
+    or negative) sets SPD_DEV_BAD_LEN in scoring, attention and verification; that
+    row gets nothing selected and o = 0 / lse = -inf, and every other row is
+    bit-identical to a run without the bad entry."""
+    import torch
+    w = _edge_workload(16, 64, lens=[40, 50, 70, 33])
+    g = Gpu(w)
+    summ = g.summarize()
+    assert g.sync_status() == 0
+    ref_sel, ref_nsel, _, _ = g.score_select(summ)
+    ref_o, ref_lse, _ = g.sparse_attn(ref_sel, ref_nsel)
+    ref_ov, ref_lv, _ = g.verify(1, q=g.d["q"].view(w.B, 1, w.H_q, w.D))
+    assert g.sync_status() == 0
+    g.d["seq_lens"][2] = w.max_pages_per_seq * w.page_size + 9 if bad == "long" else -5
+    sel, nsel, _, _ = g.score_select(summ)
+    o, lse, _ = g.sparse_attn(sel, nsel)
+    ov, lv, _ = g.verify(1, q=g.d["q"].view(w.B, 1, w.H_q, w.D))
+    assert g.sync_status() == 0x8
+    ns = nsel.cpu().numpy()
+    assert not ns[2].any()
+    assert not np_bf16(o)[2].any() and np.all(np.isneginf(lse.cpu().numpy()[2]))
+    assert not np_bf16(ov)[2].any() and np.all(np.isneginf(lv.cpu().numpy()[2]))
+    keep = [0, 1, 3]
+    assert np.array_equal(ns[keep], ref_nsel.cpu().numpy()[keep])
+    for b in keep:
+        for h in range(w.H_kv):
+            n = ns[b, h]
+            assert np.array_equal(sel.cpu().numpy()[b, h, :n], ref_sel.cpu().numpy()[b, h, :n])
+    for x, y in ((o, ref_o), (lse, ref_lse), (ov, ref_ov), (lv, ref_lv)):
+        xb = x.view(torch.int16 if x.dtype == torch.bfloat16 else torch.int32).cpu().numpy()[keep]
+        yb = y.view(torch.int16 if y.dtype == torch.bfloat16 else torch.int32).cpu().numpy()[keep]
+        assert np.array_equal(xb, yb)
+
+
 def test_bad_selection_entry_sets_status_and_does_not_fault():
     w = _edge_workload(16, 64, lens=[40, 50])
     g = Gpu(w)
