@@ -185,6 +185,13 @@ struct AttnWs {
 };
 
 // [queue: 16 B][row tickets][partial lse][partial o]; the first two must start zeroed.
+// The scores of pages_score_select start after a prefix as long as the attention
+// calls' counters (queue + tickets) and stay clear of it, so the prefix stays zero
+// and one buffer can serve the calls of a step in turn.
+static size_t score_ws_prefix(const spd_dims* dims) {
+    return align256(16 + (size_t)dims->B * dims->H_kv * sizeof(int));
+}
+
 AttnWs attn_ws_layout(void* ws, long long rows, int S, int R, int D) {
     AttnWs w;
     size_t off = 0;
@@ -229,8 +236,7 @@ SPD_API spd_status spd_device_status(uint32_t* out, int32_t clear) {
 
 SPD_API size_t spd_score_select_workspace_size(const spd_dims* dims) {
     if (check_dims(dims) != SPD_OK) return 0;
-    const long long rows = (long long)dims->B * dims->H_kv;
-    return align256((size_t)rows * dims->max_pages_per_seq * sizeof(float));  // the scores
+    return score_ws_prefix(dims) + (size_t)dims->B * dims->H_kv * dims->max_pages_per_seq * sizeof(float);
 }
 
 SPD_API size_t spd_sparse_decode_workspace_size(const spd_dims* dims, int32_t k_max, int32_t num_splits) {
@@ -392,7 +398,7 @@ static spd_status score_select_setup(const spd_dims* dims, const spd_bf16* q, co
     a.sel = sel;
     a.nsel = nsel;
     a.k_max = k_max;
-    a.scores = scores ? scores : static_cast<float*>(ws);
+    a.scores = scores ? scores : reinterpret_cast<float*>(static_cast<char*>(ws) + score_ws_prefix(dims));
     a.B = dims->B;
     a.H_q = dims->H_q;
     a.H_kv = dims->H_kv;

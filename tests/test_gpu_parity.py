@@ -305,6 +305,47 @@ def test_dense_all_pages_equals_sparse_all_pages():
     assert np.abs(lse_s.cpu().numpy() - lse_d.cpu().numpy()[:, 0]).max() <= 1e-3
 
 
+@pytest.mark.parametrize("key", ["q8b", "tiny"])
+def test_one_workspace_serves_the_calls_in_turn(key):
+    """One zeroed buffer of the largest workspace size serves scoring + selection,
+    sparse attention and verification one after the other, twice (each call leaves
+    the counters the others need at zero): results bit-identical to separate
+    workspaces."""
+    import torch
+    import sparse_attention_decode_pages_gb300 as spd
+    w = small(key)
+    g = Gpu(w)
+    summ = g.summarize()
+    sel0, nsel0, _, _ = g.score_select(summ)
+    o0, lse0, _ = g.sparse_attn(sel0, nsel0)
+    qv = g.d["q"].view(w.B, 1, w.H_q, w.D)
+    ov0, lv0, _ = g.verify(1, q=qv)
+    ws = g.ws(max(spd.spd_score_select_workspace_size(g.dims),
+                  spd.spd_sparse_decode_workspace_size(g.dims, w.k_max, 0),
+                  spd.spd_dense_verify_workspace_size(g.dims, 1, 0)))
+    d = g.d
+    for _ in range(2):
+        sel = torch.full_like(sel0, -1)
+        nsel = torch.full_like(nsel0, -7)
+        o = torch.full_like(o0, float("nan"))
+        lse = torch.full_like(lse0, float("nan"))
+        ov = torch.full_like(ov0, float("nan"))
+        lv = torch.full_like(lv0, float("nan"))
+        spd.pages_score_select(g.dims, d["q"], summ, d["seq_lens"], w.policy, sel, nsel, w.k_max, ws)
+        spd.sparse_decode_attn(g.dims, d["q"], d["K"], d["V"], d["page_table"], d["seq_lens"], sel, nsel,
+                               w.k_max, o, ws, lse=lse)
+        spd.dense_verify_attn(g.dims, 1, qv, d["K"], d["V"], d["page_table"], d["seq_lens"], ov, ws, lse=lv)
+        assert g.sync_status() == 0
+        assert torch.equal(nsel, nsel0)
+        for b in range(w.B):
+            for h in range(w.H_kv):
+                n = int(nsel0[b, h])
+                assert torch.equal(sel[b, h, :n], sel0[b, h, :n])
+        for x, y in ((o, o0), (lse, lse0), (ov, ov0), (lv, lv0)):
+            assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32),
+                               y.view(torch.int16) if y.dtype == torch.bfloat16 else y.view(torch.int32))
+
+
 def test_workspace_sizes_do_not_change_after_first_launch():
     """Auto split counts (and so workspace sizes) are the same before and after launches."""
     w = small("q8b")
