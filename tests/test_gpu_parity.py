@@ -163,6 +163,51 @@ def test_identical_pages_tie_to_lower_ids():
         assert sel.cpu().numpy()[0, h, : nsel[0, h]].tolist() == [0, 1, 2, 3, 11]
 
 
+def test_more_tied_pages_than_are_ranked_take_the_lowest_ids():
+    """300 identical pages (more tied candidates than the selection ranks pairwise):
+    the exact-key path takes the lowest page ids after the mandatory ones."""
+    n, D = 16 * 300, 64
+    k = np.random.default_rng(5).standard_normal(D).astype(np.float32)
+    K = [np.tile(k, (n, 2, 1))]
+    pol = wl.BudgetPolicy("fixed", fixed_pages=20, sink_pages=1, local_pages=2)
+    w = custom([n], 4, 2, D, 16, K=K, policy=pol, k_max=24, rng=np.random.default_rng(6))
+    g = Gpu(w)
+    sel, nsel, _, _ = g.score_select(g.summarize())
+    assert g.sync_status() == 0
+    for h in range(2):
+        assert sel.cpu().numpy()[0, h, : nsel[0, h]].tolist() == list(range(18)) + [298, 299]
+
+
+@pytest.mark.parametrize("top_p", [None, 0.8])
+def test_scores_of_both_signs_select_as_the_oracle(top_p):
+    """Pages whose scores straddle zero (keys +-(1 + p/97) times one vector, so every
+    candidate's score is distinct and the order-preserving keys differ in the sign
+    bit): the radix select and the top-p descent agree with the oracle."""
+    import dataclasses
+    ps, D, P = 16, 64, 150
+    rng = np.random.default_rng(8)
+    base = rng.standard_normal(D).astype(np.float32)
+    K = []
+    for _ in range(2):
+        rows = []
+        for p in range(P):
+            sgn = 1.0 if (p * 7) % 3 else -1.0
+            rows.append(np.tile(sgn * (1.0 + p / 97.0) * base, (ps, 2, 1)))
+        K.append(np.concatenate(rows).astype(np.float32))
+    pol = wl.BudgetPolicy("fixed", fixed_pages=23, sink_pages=1, local_pages=3)
+    if top_p is not None:
+        pol = dataclasses.replace(pol, mode="top_p", top_p=top_p, score_scale=0.125)
+    w = custom([P * ps, P * ps - 5], 4, 2, D, ps, K=K, policy=pol, k_max=P, rng=rng)
+    ref = oracle.decode_step(w, threads=4)
+    g = Gpu(w)
+    sel, nsel, sc, _ = g.score_select(g.summarize())
+    assert g.sync_status() == 0
+    sc_g = sc.cpu().numpy()
+    assert (sc_g[:, :, :P] < 0).any() and (sc_g[:, :, :P] > 0).any()
+    compare_selection(w, sel.cpu().numpy(), nsel.cpu().numpy(), sc_g.astype(np.float64), ref["sel"],
+                      ref["nsel"], ref["scores"])
+
+
 def test_bad_page_id_sets_status_and_does_not_fault():
     w = _edge_workload(16, 64, lens=[40, 50])
     w.page_table[1, 1] = w.num_phys_pages + 5
