@@ -12,8 +12,10 @@
 // products are exact in fp32; accumulation is fp32.
 //
 // Work layout: a persistent grid (three CTAs of 4 warps per SM).  All 16-page
-// tiles of all (sequence, KV head) rows are numbered in one sequence and every
-// warp takes an equal contiguous share, so the work is balanced to a tile.
+// tiles of all (sequence, KV head) rows are numbered in one sequence (a row's
+// from its last page down) and every warp takes an equal contiguous share, so
+// the work is balanced to a tile; in the chained step the warps instead take
+// 4-tile chunks from a counter in row order and count finished tiles per row.
 // The summaries are stored sequence-major, so a tile is one contiguous 8 KB
 // run: every warp owns a 2-slot ring of shared-memory slots filled by one 1-D
 // bulk copy per tile (completion counted on the slot's mbarrier) ahead of the
@@ -31,9 +33,9 @@
 // agree), so it already spreads them; as soon as the digit being refined holds
 // at most 256 keys (after one pass, typically) those keys are ranked pairwise
 // by (key desc, page asc) instead; otherwise the passes end on the exact k'-th
-// key.  Pages above the boundary plus the
-// boundary pages that rank (or, at an exact key, the lowest-id pages equal to
-// it) are compacted in ascending order into sel[] with ballots.
+// key.  Pages above the boundary plus the boundary pages that rank (or, at an
+// exact key, the lowest-id pages equal to it) are compacted in ascending order
+// into sel[] with ballots.
 #include "common.cuh"
 #include "kernels.h"
 
