@@ -566,9 +566,13 @@ def cpu_baseline(w, T, min_seconds=3.0):
         el = time.perf_counter() - t0
         if el >= min_seconds:
             break
+    t1 = time.perf_counter()
+    _oracle_sparse_step(w, summ, 1)  # the same pass on one thread
+    el1 = time.perf_counter() - t1
     return {"value": n * w.B / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"{n} full passes of scores + selection + sparse attention over the whole "
-                      f"batch (B={w.B}); page summaries precomputed once outside the timing"}
+                      f"batch (B={w.B}); page summaries precomputed once outside the timing",
+            "single_thread": {"value": w.B / el1, "unit": "tokens/s", "sample": "one full pass on 1 thread"}}
 
 
 def run_reference(args):
