@@ -17,18 +17,20 @@ import math
 import os
 
 __all__ = [
-    "SpdError", "Dims", "Policy", "lib", "dims_of", "policy_of", "workspace",
-    "pages_summarize", "pages_score_select", "sparse_decode_attn", "dense_verify_attn",
-    "sparse_decode_attn_noalloc",
-    "lse_merge", "spd_device_status", "spd_score_select_workspace_size",
+    "SpdError", "Dims", "Policy", "RoundDesc", "Round", "lib", "dims_of", "policy_of", "workspace",
+    "pages_summarize", "kv_append_refresh", "pages_score_select", "pages_append_score_select",
+    "sparse_decode_attn", "sparse_decode_attn_noalloc", "sparse_decode_step", "dense_verify_attn",
+    "lse_merge", "spec_accept", "spd_device_status", "spd_score_select_workspace_size",
     "spd_sparse_decode_workspace_size", "spd_dense_verify_workspace_size",
-    "DEV_BAD_PAGE", "DEV_BAD_SEL", "DEV_TIMEOUT",
+    "spd_sparse_decode_step_workspace_size",
+    "DEV_BAD_PAGE", "DEV_BAD_SEL", "DEV_TIMEOUT", "DEV_BAD_LEN", "DEV_BAD_TOKEN",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libspd.so")
 
-DEV_BAD_PAGE, DEV_BAD_SEL, DEV_TIMEOUT = 0x1, 0x2, 0x4
+# device status bits (SPD_DEV_* in include/spd.h)
+DEV_BAD_PAGE, DEV_BAD_SEL, DEV_TIMEOUT, DEV_BAD_LEN, DEV_BAD_TOKEN = 0x1, 0x2, 0x4, 0x8, 0x10
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "WORKSPACE"}
 _MODES = {"fixed": 0, "linear": 1, "fraction": 2, "top_p": 3}
 
@@ -166,15 +168,18 @@ def _size(v: int, what: str) -> int:
 
 
 def spd_score_select_workspace_size(dims: Dims) -> int:
+    """Bytes of workspace pages_score_select needs for these dims."""
     return _size(lib().spd_score_select_workspace_size(ctypes.byref(dims)), "score_select workspace")
 
 
 def spd_sparse_decode_workspace_size(dims: Dims, k_max: int, num_splits: int = 0) -> int:
+    """Bytes of workspace sparse_decode_attn needs (num_splits 0: the automatic split count)."""
     return _size(lib().spd_sparse_decode_workspace_size(ctypes.byref(dims), k_max, num_splits),
                  "sparse_decode workspace")
 
 
 def spd_dense_verify_workspace_size(dims: Dims, T: int, num_splits: int = 0) -> int:
+    """Bytes of workspace dense_verify_attn needs for T positions."""
     return _size(lib().spd_dense_verify_workspace_size(ctypes.byref(dims), T, num_splits),
                  "dense_verify workspace")
 
@@ -186,12 +191,14 @@ def workspace(nbytes: int, device=None):
 
 
 def spd_device_status(clear: bool = False) -> int:
+    """The device status word (DEV_* bits raised by kernels since the last clear); waits for the device."""
     v = ctypes.c_uint32(0)
     _check(lib().spd_device_status(ctypes.byref(v), 1 if clear else 0))
     return v.value
 
 
 def pages_summarize(dims: Dims, K, page_table, seq_lens, summ, only_pages=None, stream=None):
+    """Per-page key min / max summaries into summ (all pages, or the listed b * max_pages + p slots)."""
     n_only = 0 if only_pages is None else only_pages.numel()
     _check(lib().pages_summarize(ctypes.byref(dims), _ptr(K), _ptr(page_table), _ptr(seq_lens),
                                  _ptr(only_pages), n_only, _ptr(summ), _stream(stream)))
@@ -199,6 +206,7 @@ def pages_summarize(dims: Dims, K, page_table, seq_lens, summ, only_pages=None, 
 
 def kv_append_refresh(dims: Dims, T: int, K, V, page_table, seq_lens, k_new, v_new, summ,
                       stream=None):
+    """Write the T newest tokens into the paged cache and rebuild the summaries of their pages."""
     _check(lib().kv_append_refresh(ctypes.byref(dims), T, _ptr(K), _ptr(V), _ptr(page_table),
                                    _ptr(seq_lens), _ptr(k_new), _ptr(v_new), _ptr(summ),
                                    _stream(stream)))
@@ -213,6 +221,7 @@ def spec_accept(p_draft, q_target, draft, u_acc, u_res, n_accepted, tokens, stre
 
 def pages_append_score_select(dims: Dims, K, V, page_table, seq_lens, k_new, v_new, q, summ, policy,
                               sel, nsel, k_max: int, ws, scores=None, stream=None):
+    """kv_append_refresh (T = 1) fused into pages_score_select's pass over the summaries."""
     pol = policy if isinstance(policy, Policy) else policy_of(policy)
     _check(lib().pages_append_score_select(ctypes.byref(dims), _ptr(K), _ptr(V), _ptr(page_table),
                                            _ptr(seq_lens), _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(summ),
@@ -221,11 +230,13 @@ def pages_append_score_select(dims: Dims, K, V, page_table, seq_lens, k_new, v_n
 
 
 def spd_sparse_decode_step_workspace_size(dims: Dims, k_max: int) -> int:
+    """Bytes of workspace sparse_decode_step needs."""
     return _size(lib().spd_sparse_decode_step_workspace_size(ctypes.byref(dims), k_max), "decode step workspace")
 
 
 def sparse_decode_step(dims: Dims, K, V, page_table, seq_lens, k_new, v_new, q, summ, policy, sel, nsel,
                        k_max: int, o, ws, lse=None, softmax_scale: float | None = None, stream=None):
+    """Append (k_new / v_new may be None) + score + select + sparse attention in one call."""
     pol = policy if isinstance(policy, Policy) else policy_of(policy)
     scale = 1.0 / math.sqrt(dims.D) if softmax_scale is None else softmax_scale
     _check(lib().sparse_decode_step(ctypes.byref(dims), _ptr(K), _ptr(V), _ptr(page_table), _ptr(seq_lens),
@@ -236,6 +247,7 @@ def sparse_decode_step(dims: Dims, K, V, page_table, seq_lens, k_new, v_new, q, 
 
 def pages_score_select(dims: Dims, q, summ, seq_lens, policy, sel, nsel, k_max: int, ws,
                        scores=None, stream=None):
+    """Page upper-bound scores and the budgeted selection (ascending page ids) per (sequence, KV head)."""
     pol = policy if isinstance(policy, Policy) else policy_of(policy)
     _check(lib().pages_score_select(ctypes.byref(dims), _ptr(q), _ptr(summ), _ptr(seq_lens),
                                     ctypes.byref(pol), _ptr(sel), _ptr(nsel), k_max,
@@ -245,6 +257,7 @@ def pages_score_select(dims: Dims, q, summ, seq_lens, policy, sel, nsel, k_max: 
 def sparse_decode_attn(dims: Dims, q, K, V, page_table, seq_lens, sel, nsel, k_max: int, o, ws,
                        lse=None, num_splits: int = 0, softmax_scale: float | None = None,
                        stream=None):
+    """Attention of the decode query over the selected pages (split-K, merged)."""
     scale = 1.0 / math.sqrt(dims.D) if softmax_scale is None else softmax_scale
     _check(lib().sparse_decode_attn(ctypes.byref(dims), _ptr(q), _ptr(K), _ptr(V), _ptr(page_table),
                                     _ptr(seq_lens), _ptr(sel), _ptr(nsel), k_max, num_splits,
@@ -265,6 +278,7 @@ def sparse_decode_attn_noalloc(dims: Dims, q, K, V, page_table, seq_lens, sel, n
 
 def dense_verify_attn(dims: Dims, T: int, q, K, V, page_table, seq_lens, o, ws, lse=None,
                       num_splits: int = 0, softmax_scale: float | None = None, stream=None):
+    """Causal attention of the T newest positions over the whole cache."""
     scale = 1.0 / math.sqrt(dims.D) if softmax_scale is None else softmax_scale
     _check(lib().dense_verify_attn(ctypes.byref(dims), T, _ptr(q), _ptr(K), _ptr(V),
                                    _ptr(page_table), _ptr(seq_lens), num_splits, scale, _ptr(o),
@@ -272,6 +286,7 @@ def dense_verify_attn(dims: Dims, T: int, q, K, V, page_table, seq_lens, o, ws, 
 
 
 def lse_merge(part_o, part_lse, o, lse=None, stream=None):
+    """Merge split partials (part_o [S][rows][D], part_lse [S][rows]) by the log-sum-exp rule."""
     S, rows, D = part_o.shape
     _check(lib().lse_merge(S, rows, D, _ptr(part_o), _ptr(part_lse), _ptr(o), _ptr(lse),
                            _stream(stream)))
