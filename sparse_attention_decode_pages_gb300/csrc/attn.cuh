@@ -179,7 +179,9 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
                 (void)ld_acquire(a.sel_done + row);
                 __syncwarp();
                 if (lane == 0) {
-                    a.sel_done[row] = 0u;  // consumed (one unit per row in a chained step)
+                    // each of the row's num_splits units reads the flag once (counting
+                    // up from 1); the last reader clears it for the next call
+                    if (atomicAdd(a.sel_done + row, 1u) == (unsigned)a.num_splits) a.sel_done[row] = 0u;
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                 }
             }

@@ -115,6 +115,39 @@ __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
 // __threadfence): followed by a relaxed write it forms a release pattern.
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// Relaxed (morally strong, unordered) accesses at GPU scope: a value another CTA
+// polls is stored and loaded with these (the load bypasses L1).
+__device__ __forceinline__ void st_relaxed(unsigned* p, unsigned v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Fire-and-forget add at GPU scope with no ordering: a progress hint, not a
+// release (the data it announces carries its own readiness).
+__device__ __forceinline__ void red_relaxed_add(unsigned* p, unsigned v) {
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// As flag_wait_bounded, with relaxed loads (no ordering: for a progress count
+// whose data is checked on its own).
+__device__ __forceinline__ bool count_wait_bounded(const unsigned* cnt, unsigned value, unsigned* status) {
+    if (ld_relaxed(cnt) >= value) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(64);
+        if (ld_relaxed(cnt) >= value) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            raise_status(status, SPD_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 __device__ __forceinline__ bool flag_wait_bounded(const unsigned* flag, unsigned value, unsigned* status) {
     if (ld_acquire(flag) >= value) return true;
     const unsigned long long t0 = globaltimer_ns();

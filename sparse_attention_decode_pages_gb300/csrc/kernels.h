@@ -93,13 +93,16 @@ struct ScoreSelectArgs {
     const uint16_t* k_new;  // [B][H_kv][D]
     const uint16_t* v_new;
     uint16_t* summ_w;       // == summ
-    // Chained step (sparse_decode_step): tiles are handed out in row order from a
-    // counter, each finished tile is counted per row, and the selection of a row
+    // Chained step (sparse_decode_step): tiles are handed out in row order from
+    // counters, each finished tile is counted per row, and the selection of a row
     // starts when its count is complete (instead of after the whole scoring grid).
-    unsigned long long* tile_ctr;  // NULL: static partition of the tiles
+    unsigned long long* tile_ctr;  // [2]: chunk and single-tile counters, zero on entry and on exit
     unsigned* warps_done;
-    unsigned* tiles_done;          // [B*H_kv], zero on entry and on exit
+    unsigned* tiles_done;          // [B*H_kv] progress hints (NULL: not chained), zero on entry and on exit
     unsigned* sel_done;            // [B*H_kv]: set when a row's selection is written
+    // [B*H_kv][max_pages] order-preserving score keys (never 0), zero on entry and
+    // on exit: a key is its own ready flag, so the scoring warps need no fences
+    unsigned* keys;
 };
 // Scores every page (persistent grid sized to num_sms), then selects per row.
 cudaError_t launch_score_select(const ScoreSelectArgs& a, int num_sms, cudaStream_t st);

@@ -15,7 +15,8 @@
 // tiles of all (sequence, KV head) rows are numbered in one sequence (a row's
 // from its last page down) and every warp takes an equal contiguous share, so
 // the work is balanced to a tile; in the chained step the warps instead take
-// 4-tile chunks from a counter in row order and count finished tiles per row.
+// 4-tile chunks from a counter in row order (single tiles at the end, so they
+// finish within about a tile of each other) and count finished tiles per row.
 // The summaries are stored sequence-major, so a tile is one contiguous 8 KB
 // run: every warp owns a 2-slot ring of shared-memory slots filled by one 1-D
 // bulk copy per tile (completion counted on the slot's mbarrier) ahead of the
@@ -24,16 +25,15 @@
 // the query operand uses the same order (the contraction is a sum, so any
 // common order is exact), so no shuffles or ldmatrix are needed.
 //
-// Selection (a second kernel; a CTA per (sequence, KV head) row, or in the
-// chained step two persistent CTAs per SM taking the rows in order): the
-// mandatory pages, then the k'-th best score by a radix select over
-// order-preserving uint32 keys (shared-memory histogram with warp-aggregated
-// atomics, since neighbouring scores share bins).  The first digit is the 8
-// bits below those all candidates share (where their minimum and maximum
+// Selection (a second kernel; a 256-thread CTA per (sequence, KV head) row, or
+// in the chained step two persistent 128-thread CTAs per SM taking the rows in
+// order): the mandatory pages, then the k'-th best score by a radix select over
+// order-preserving uint32 keys (shared-memory histogram).  The first digit is
+// the 8 bits below those all candidates share (where their minimum and maximum
 // agree), so it already spreads them; as soon as the digit being refined holds
-// at most 256 keys (after one pass, typically) those keys are ranked pairwise
-// by (key desc, page asc) instead; otherwise the passes end on the exact k'-th
-// key.  Pages above the boundary plus the boundary pages that rank (or, at an
+// at most as many keys as the CTA has threads (after one pass, typically)
+// those keys are ranked pairwise by (key desc, page asc) instead; otherwise the
+// passes end on the exact k'-th key.  Pages above the boundary plus the boundary pages that rank (or, at an
 // exact key, the lowest-id pages equal to it) are compacted in ascending order
 // into sel[] with ballots.
 #include "common.cuh"
@@ -44,7 +44,8 @@ namespace spd {
 constexpr int kScoreWarps = 4;
 constexpr int kScoreThreads = 32 * kScoreWarps;
 constexpr int kScoreStages = 2;
-constexpr int kChunkTiles = 4;  // chained step: tiles taken from the counter at a time
+constexpr int kChunkTiles = 4;  // chained step: consecutive tiles a warp takes at a time
+constexpr int kTailTiles = 2;   // chained step: tiles per warp handed out singly at the end
 
 template <int D>
 struct ScoreCfg {
@@ -65,11 +66,12 @@ __device__ __forceinline__ long long budget_pages(const spd_budget_policy& pol, 
     return (len * pol.frac_num + pol.frac_den * ps - 1) / (pol.frac_den * ps);
 }
 
-constexpr int kSelWarps = 8;
-constexpr int kSelThreads = 32 * kSelWarps;
-// Once the radix digit being refined holds at most this many candidates, they
-// are ranked directly (pairwise) instead of refining further digits.
-constexpr int kRankMax = kSelThreads;
+// Selection CTAs: 256 threads for one row after the scoring grid, 128 in the
+// chained step (two per SM fit beside the three scoring CTAs).  Once the radix
+// digit being refined holds at most NT candidates, they are ranked directly
+// (pairwise, a thread each) instead of refining further digits.
+constexpr int kSelThreads = 256;
+constexpr int kSelThreadsChained = 128;
 
 __device__ __forceinline__ float key_float(uint32_t u) {
     return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
@@ -100,13 +102,13 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
 // wts).  The k'-th page is found by a radix descent over the keys in which each
 // bin carries its count and its weight, starting below the bits all candidates
 // share (kmin / kmax: their smallest and largest key).
-template <class Mand>
+template <int NT, class Mand>
 __device__ int top_p_pages(const ScoreSelectArgs& a, const uint32_t* keys, int P, Mand mand,
                            uint32_t* hist, int& s_digit, int& s_rem, uint32_t kmin, uint32_t kmax,
                            uint32_t* wts) {
     typedef unsigned long long u64;
     __shared__ u64 mhist[256];
-    __shared__ u64 red[kSelWarps];
+    __shared__ u64 red[NT / 32];
     __shared__ u64 s_mass;
     __shared__ uint32_t s_kmax;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -114,7 +116,7 @@ __device__ int top_p_pages(const ScoreSelectArgs& a, const uint32_t* keys, int P
     if (tid == 0) s_kmax = 0;
     __syncthreads();
     uint32_t km = 0;
-    for (int p = tid; p < P; p += kSelThreads) km = max(km, keys[p]);
+    for (int p = tid; p < P; p += NT) km = max(km, keys[p]);
 #pragma unroll
     for (int off = 16; off; off >>= 1) km = max(km, __shfl_xor_sync(0xffffffffu, km, off));
     if (lane == 0) atomicMax(&s_kmax, km);
@@ -122,7 +124,7 @@ __device__ int top_p_pages(const ScoreSelectArgs& a, const uint32_t* keys, int P
     const float smax = key_float(s_kmax);
     const float c2 = a.pol.score_scale * 1.4426950408889634f;
     u64 tot = 0, man = 0;
-    for (int p = tid; p < P; p += kSelThreads) {
+    for (int p = tid; p < P; p += NT) {
         const uint32_t w = page_weight(keys[p], smax, c2);
         wts[p] = w;
         tot += w;
@@ -146,10 +148,12 @@ __device__ int top_p_pages(const ScoreSelectArgs& a, const uint32_t* keys, int P
         const int wd = h + 1 < 8 ? h + 1 : 8;
         const int shift = h + 1 - wd;
         const uint32_t dmask = (1u << wd) - 1u;
-        hist[tid] = 0;
-        mhist[tid] = 0;
+        for (int i = tid; i < 256; i += NT) {
+            hist[i] = 0;
+            mhist[i] = 0;
+        }
         __syncthreads();
-        for (int p0 = 0; p0 < P; p0 += kSelThreads) {
+        for (int p0 = 0; p0 < P; p0 += NT) {
             const int p = p0 + tid;
             bool in = false;
             uint32_t bin = 0, w = 0;
@@ -234,15 +238,55 @@ __device__ int top_p_pages(const ScoreSelectArgs& a, const uint32_t* keys, int P
     return n_above + (int)min((u64)eq_count, t);
 }
 
+// Chained step: copies the row's P keys from global (kg) into shared memory (ks),
+// thread `me` of `NT` taking every NT-th key; the loads of a batch are issued
+// back to back before any is used.  True if this thread saw a key still 0 (not
+// yet written by the scoring).
+template <int NT>
+__device__ __forceinline__ bool gather_keys(const unsigned* kg, uint32_t* ks, int P, int me) {
+    constexpr int BATCH = 8;
+    bool missing = false;
+    for (int p0 = 0; p0 < P; p0 += NT * BATCH) {
+        unsigned u[BATCH];
+#pragma unroll
+        for (int i = 0; i < BATCH; ++i) {
+            const int p = p0 + i * NT + me;
+            u[i] = p < P ? ld_relaxed(kg + p) : 1u;
+        }
+#pragma unroll
+        for (int i = 0; i < BATCH; ++i) {
+            const int p = p0 + i * NT + me;
+            if (p < P) ks[p] = u[i];
+            missing |= (u[i] == 0u);
+        }
+    }
+    return missing;
+}
+
+// Reads again the keys still 0 in shared memory; true if one still is.
+__device__ __forceinline__ bool repoll_keys(const unsigned* kg, uint32_t* ks, int P, int me, int nt) {
+    bool missing = false;
+    for (int p = me; p < P; p += nt) {
+        if (ks[p] == 0u) {
+            const unsigned u = ld_relaxed(kg + p);
+            ks[p] = u;
+            missing |= (u == 0u);
+        }
+    }
+    return missing;
+}
+
 // Selection of one (sequence, KV head) row by a CTA of 8 warps.  keys: the
 // dynamic shared memory (the row's order-preserving score keys, then bit words).
+template <int NT>
 __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const int row, uint32_t* keys) {
+    constexpr int NWARP = NT / 32;
     __shared__ uint32_t hist[256];
     __shared__ int s_digit, s_rem, s_cnt, s_ncol;
     __shared__ uint32_t s_kmin, s_kmax;
-    __shared__ int w_eq[kSelWarps], w_take[kSelWarps];
-    __shared__ uint32_t col_key[kRankMax];
-    __shared__ int col_p[kRankMax];
+    __shared__ int w_eq[NWARP], w_take[NWARP];
+    __shared__ uint32_t col_key[NT];
+    __shared__ int col_p[NT];
     // after the keys: boundary pages chosen by rank, and the final decision (bit per page)
     uint32_t* s_chosen = keys + a.max_pages;
     uint32_t* s_take = s_chosen + (a.max_pages + 31) / 32;
@@ -250,20 +294,39 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
     const unsigned lt_mask = (1u << lane) - 1u;
     const int b = row / a.H_kv;
     __shared__ int s_ok;
-    if (a.tiles_done) {
-        // chained step: wait for this row's tiles only, not for the whole scoring grid
-        if (tid == 0) {
-            const int P0 = max(0, seq_pages(a.seq_lens[b], a.ps, a.max_pages));  // as the scoring kernel counts
-            s_ok = flag_wait_bounded(a.tiles_done + row, (unsigned)((P0 + 15) / 16), a.status);
-            if (s_ok) a.tiles_done[row] = 0u;  // this row's count is consumed
-        }
+    if (a.keys) {
+        // chained step: wait for this row's tiles only, not for the whole scoring grid.
+        // The count is a hint (an unordered add); each key is its own ready flag, so
+        // the keys are gathered into shared memory and any still 0 is read again.
+        const int P0 = max(0, seq_pages(a.seq_lens[b], a.ps, a.max_pages));  // as the scoring kernel counts
+        if (tid == 0) s_ok = count_wait_bounded(a.tiles_done + row, (unsigned)((P0 + 15) / 16), a.status);
         __syncthreads();
         if (!s_ok) return;
+        unsigned* kg = a.keys + (long long)row * a.max_pages;
+        const unsigned long long t0 = globaltimer_ns();
+        bool missing = gather_keys<NT>(kg, keys, P0, tid);
+        while (true) {
+            if (!__syncthreads_or(missing)) break;
+            if (tid == 0) {
+                s_ok = globaltimer_ns() - t0 <= kWaitLimitNs;
+                if (!s_ok) raise_status(a.status, SPD_DEV_TIMEOUT);
+            }
+            __syncthreads();
+            if (!s_ok) return;
+            __nanosleep(64);
+            missing = repoll_keys(kg, keys, P0, tid, NT);
+        }
+        // acquire: the fused append's writes, released before its tile's keys, are
+        // visible from here on (and, through the publish below, to the attention)
+        fence_acq_rel_gpu();
+        for (int p = tid; p < P0; p += NT) kg[p] = 0u;  // zero again for the next call
+        if (tid == 0) a.tiles_done[row] = 0u;                     // this row's count is consumed
     }
     // chained step: the row's selection is published to the attention kernel
+    // (the barrier orders every thread's writes before thread 0's release, which is
+    // cumulative over them: one release store publishes the whole row)
     auto publish = [&]() {
         if (!a.sel_done) return;
-        fence_acq_rel_gpu();
         __syncthreads();
         if (tid == 0) st_release(a.sel_done + row, 1u);
     };
@@ -290,24 +353,34 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
         s_kmax = 0u;
     }
     __syncthreads();
-    const float* sc = a.scores + (long long)row * a.max_pages;
     uint32_t kmin = 0xffffffffu, kmax = 0u;
-    for (int p0 = 0; p0 < P; p0 += kSelThreads * 4) {
-        float v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int p = p0 + i * kSelThreads + tid;
-            v[i] = p < P ? sc[p] : 0.f;
+    if (a.keys) {  // chained step: the keys are already in shared memory
+        for (int p = tid; p < P; p += NT) {
+            const uint32_t u = keys[p];
+            if (!mand(p)) {
+                kmin = min(kmin, u);
+                kmax = max(kmax, u);
+            }
         }
+    } else {
+        const float* sc = a.scores + (long long)row * a.max_pages;
+        for (int p0 = 0; p0 < P; p0 += NT * 4) {
+            float v[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int p = p0 + i * kSelThreads + tid;
-            if (p < P) {
-                const uint32_t u = float_key(v[i]);
-                keys[p] = u;
-                if (!mand(p)) {
-                    kmin = min(kmin, u);
-                    kmax = max(kmax, u);
+            for (int i = 0; i < 4; ++i) {
+                const int p = p0 + i * NT + tid;
+                v[i] = p < P ? sc[p] : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int p = p0 + i * NT + tid;
+                if (p < P) {
+                    const uint32_t u = float_key(v[i]);
+                    keys[p] = u;
+                    if (!mand(p)) {
+                        kmin = min(kmin, u);
+                        kmax = max(kmax, u);
+                    }
                 }
             }
         }
@@ -322,7 +395,7 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
 
     long long k;
     if (a.pol.mode == SPD_BUDGET_TOP_P)
-        k = nm + top_p_pages(a, keys, P, mand, hist, s_digit, s_rem, s_kmin, s_kmax,
+        k = nm + top_p_pages<NT>(a, keys, P, mand, hist, s_digit, s_rem, s_kmin, s_kmax,
                              s_take + (a.max_pages + 31) / 32);
     else
         k = budget_pages(a.pol, len, a.ps);
@@ -347,18 +420,18 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
         // The bits above h are the same in every candidate (their minimum and maximum
         // agree there): the radix starts below them, so the first digit already
         // spreads the keys.  Digits of up to 8 bits until the boundary digit holds at
-        // most kRankMax keys (then ranked) or every bit is refined (an exact key).
+        // most NT keys (then ranked) or every bit is refined (an exact key).
         int h = 31 - __clz((int)(s_kmin ^ s_kmax));  // -1 when all candidates are equal
         pmask = h < 0 ? 0xffffffffu : (h >= 31 ? 0u : ~((2u << h) - 1u));
         prefix = s_kmin & pmask;
         int ncnt = ncand;
-        while (h >= 0 && ncnt > kRankMax) {
+        while (h >= 0 && ncnt > NT) {
             const int wd = h + 1 < 8 ? h + 1 : 8;
             const int shift = h + 1 - wd;
             const uint32_t dmask = (1u << wd) - 1u;
-            hist[tid] = 0;  // kSelThreads == 256 bins
+            for (int i = tid; i < 256; i += NT) hist[i] = 0;
             __syncthreads();
-            for (int p0 = 0; p0 < P; p0 += kSelThreads) {
+            for (int p0 = 0; p0 < P; p0 += NT) {
                 const int p = p0 + tid;
                 bool in = false;
                 uint32_t bin = 0;
@@ -367,11 +440,9 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
                     in = (u & pmask) == prefix;
                     bin = (u >> shift) & dmask;
                 }
-                const unsigned act = __ballot_sync(0xffffffffu, in);
-                if (in) {  // neighbouring scores share bins: one atomic per distinct bin
-                    const unsigned same = __match_any_sync(act, bin);
-                    if (lane == __ffs(same) - 1) atomicAdd(hist + bin, (uint32_t)__popc(same));
-                }
+                // below the bits every candidate shares the keys spread over the bins,
+                // so a plain shared atomic per key rarely conflicts
+                if (in) atomicAdd(hist + bin, 1u);
             }
             __syncthreads();
             if (warp == 0) {
@@ -413,21 +484,21 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
             ncnt = s_cnt;
             h = shift - 1;
         }
-        ranked = ncnt <= kRankMax;  // block-uniform
+        ranked = ncnt <= NT;  // block-uniform
         thr = prefix;
     }
     if (ranked) {
         // The candidates whose key matches the refined prefix, ranked by (key desc,
         // page asc); the first `rem` of them are chosen.
-        for (int w = tid; w < (P + 31) / 32; w += kSelThreads) s_chosen[w] = 0u;
+        for (int w = tid; w < (P + 31) / 32; w += NT) s_chosen[w] = 0u;
         if (tid == 0) s_ncol = 0;
         __syncthreads();
-        for (int p = tid; p < P; p += kSelThreads) {
+        for (int p = tid; p < P; p += NT) {
             if (mand(p)) continue;
             const uint32_t u = keys[p];
             if ((u & pmask) != prefix) continue;
             const int at = atomicAdd(&s_ncol, 1);
-            col_key[at] = u;  // at < s_cnt <= kRankMax
+            col_key[at] = u;  // at < s_cnt <= NT
             col_p[at] = p;
         }
         __syncthreads();
@@ -448,7 +519,7 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
     // Ascending compaction: mandatory pages, keys above the threshold, and the
     // first `rem` keys equal to it in page order.  Warp w owns a contiguous
     // segment of pages; per-warp counts are scanned through shared memory.
-    const int seg = ((P + kSelWarps * 32 - 1) / (kSelWarps * 32)) * 32;
+    const int seg = ((P + NT - 1) / NT) * 32;
     const int lo = min(P, warp * seg), hi = min(P, lo + seg);
     auto pick = [&](int p, bool& m, bool& eq) -> bool {  // taken regardless of tie order?
         m = mand(p);
@@ -491,7 +562,7 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
     if (lane == 0) w_take[warp] = n_take;
     __syncthreads();
     int pos = 0, total = 0;
-    for (int w = 0; w < kSelWarps; ++w) {
+    for (int w = 0; w < NWARP; ++w) {
         if (w < warp) pos += w_take[w];
         total += w_take[w];
     }
@@ -509,10 +580,10 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
 }
 
 // One CTA per row, or (chained step) two CTAs per SM, each selecting rows
-// blockIdx.x, blockIdx.x + gridDim.x, ... in order: they are all resident beside
-// the scoring CTAs from the start, so the attention grid, which launches once every
-// selection CTA has started, is launched early.
-__global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) {
+// blockIdx.x, blockIdx.x + gridDim.x, ... in order (used for the top-p budget
+// and for rows too long for a warp's shared memory).
+template <int NT>
+__global__ void __launch_bounds__(NT) select_kernel(ScoreSelectArgs a) {
     extern __shared__ uint32_t keys[];
     if (a.tiles_done) {
         pdl_trigger();  // each row waits for its own tiles instead of the scoring grid
@@ -522,7 +593,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(ScoreSelectArgs a) 
     }
     const int rows = a.B * a.H_kv;
     for (int row = blockIdx.x; row < rows; row += gridDim.x) {
-        select_row_block(a, row, keys);
+        select_row_block<NT>(a, row, keys);
         __syncthreads();  // the shared state is reused by the next row
     }
 }
@@ -648,53 +719,63 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
     const long long gw = (long long)blockIdx.x * kScoreWarps + warp;
     const long long g0 = total * gw / nwarps, g1 = total * (gw + 1) / nwarps;
     // The warp's t-th tile: its t-th of an equal contiguous share, or (chained step)
-    // the next tile in row order from the shared counter, so that rows finish in
-    // order and their selection can start while later rows are still scored.
-    // Chained step: chunks of kChunkTiles consecutive tiles are taken from the counter
-    // (rows finish in order), and a warp reports finished tiles to their row once
-    // per chunk (or row change), behind one fence.
-    bool drained = false, first_chunk = true;
+    // the next tiles in row order from shared counters, so that rows finish in order
+    // and their selection can start while later rows are still scored.  Tiles
+    // [0, T1) go out in chunks of kChunkTiles (the query is reused within a chunk;
+    // warp gw's first chunk is chunk gw, with no round trip before its first copy),
+    // the last kTailTiles per warp [T1, total) one at a time from a second counter,
+    // so the warps finish within about a tile of each other.
+    const long long T1 = max(0LL, (total - nwarps * kTailTiles) / kChunkTiles * kChunkTiles);
+    int phase = 0;  // 0: first chunk, 1: chunks, 2: single tiles, 3: drained
     long long ch_cur = 0, ch_end = 0;
     auto grab = [&](int t) -> long long {
-        if (!a.tile_ctr) return g0 + t < g1 ? g0 + t : -1;
+        if (!a.tiles_done) return g0 + t < g1 ? g0 + t : -1;
         if (ch_cur < ch_end) return ch_cur++;
-        if (drained) return -1;
-        if (first_chunk) {
-            // warp gw's first chunk is chunk gw (no round trip before the first copy);
-            // the counter hands out the chunks after the first nwarps
-            first_chunk = false;
+        if (phase == 0) {
+            phase = 1;
             const long long v0 = gw * kChunkTiles;
-            if (v0 < total) {
+            if (v0 < T1) {
                 ch_cur = v0 + 1;
-                ch_end = min(v0 + kChunkTiles, total);
+                ch_end = min(v0 + kChunkTiles, T1);
                 return v0;
             }
         }
-        unsigned long long v = 0;
-        if (lane == 0) {
-            v = atomicAdd(a.tile_ctr, (unsigned long long)kChunkTiles) + (unsigned long long)(nwarps * kChunkTiles);
-            if ((long long)v >= total) {  // each warp fails exactly once; the last one resets
-                if (atomicAdd(a.warps_done, 1u) == (unsigned)nwarps - 1) {
-                    *a.tile_ctr = 0ull;
-                    *a.warps_done = 0u;
+        if (phase == 1) {
+            unsigned long long v = 0;
+            if (lane == 0)
+                v = atomicAdd(a.tile_ctr, (unsigned long long)kChunkTiles) + (unsigned long long)(nwarps * kChunkTiles);
+            v = __shfl_sync(0xffffffffu, v, 0);
+            if ((long long)v < T1) {
+                ch_cur = (long long)v + 1;
+                ch_end = min((long long)v + kChunkTiles, T1);
+                return (long long)v;
+            }
+            phase = 2;
+        }
+        if (phase == 2) {
+            unsigned long long v = 0;
+            if (lane == 0) {
+                v = T1 + atomicAdd(a.tile_ctr + 1, 1ull);
+                if ((long long)v >= total) {  // each warp runs out exactly once; the last one resets
+                    if (atomicAdd(a.warps_done, 1u) == (unsigned)nwarps - 1) {
+                        a.tile_ctr[0] = 0ull;
+                        a.tile_ctr[1] = 0ull;
+                        *a.warps_done = 0u;
+                    }
                 }
             }
+            v = __shfl_sync(0xffffffffu, v, 0);
+            if ((long long)v < total) return (long long)v;
+            phase = 3;
         }
-        v = __shfl_sync(0xffffffffu, v, 0);
-        if ((long long)v >= total) {
-            drained = true;
-            return -1;
-        }
-        ch_cur = (long long)v + 1;
-        ch_end = min((long long)v + kChunkTiles, total);
-        return (long long)v;
+        return -1;
     };
     int pend_row = -1, pend_cnt = 0;  // tiles finished but not yet reported
+    // The count only tells the selection when to start reading the row's keys (each
+    // key is its own ready flag), so it is an unordered add: no fence per chunk.
     auto report = [&]() {
         if (pend_cnt == 0) return;
-        fence_acq_rel_gpu();  // this warp's score (and append) stores before the count
-        __syncwarp();
-        if (lane == 0) atomicAdd(a.tiles_done + pend_row, (unsigned)pend_cnt);
+        if (lane == 0) red_relaxed_add(a.tiles_done + pend_row, (unsigned)pend_cnt);
         pend_cnt = 0;
     };
 
@@ -764,6 +845,9 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
         const uint8_t* sl = ring + slot * SLOT;
         if (a.K && p0 <= P - 1 && P - 1 < p0 + 16) {  // this tile holds the row's last page
             append_last_page<D>(a, b, h, a.seq_lens[b], P, ring + slot * SLOT + (P - 1 - p0) * C::PAGE_BYTES);
+            // chained step: the append's K / V / summary writes are released before
+            // this tile's keys, which the selection acquires (and the attention after it)
+            if (a.keys) fence_acq_rel_gpu();
             __syncwarp();
         }
         if (row != cur_row) {
@@ -812,10 +896,16 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
         s1 = fmaxf(s1, __shfl_xor_sync(0xffffffffu, s1, 1));
         s0 = fmaxf(s0, __shfl_xor_sync(0xffffffffu, s0, 2));
         s1 = fmaxf(s1, __shfl_xor_sync(0xffffffffu, s1, 2));
-        float* sc_row = a.scores + (long long)row * a.max_pages;
         if (c == 0) {
-            if (p0 + r < P) sc_row[p0 + r] = s0;
-            if (p0 + r + 8 < P) sc_row[p0 + r + 8] = s1;
+            if (a.keys) {  // chained step: order-preserving keys, 0 reserved for "not yet"
+                unsigned* kr = a.keys + (long long)row * a.max_pages;
+                if (p0 + r < P) st_relaxed(kr + p0 + r, max(float_key(s0), 1u));
+                if (p0 + r + 8 < P) st_relaxed(kr + p0 + r + 8, max(float_key(s1), 1u));
+            } else {
+                float* sc_row = a.scores + (long long)row * a.max_pages;
+                if (p0 + r < P) sc_row[p0 + r] = s0;
+                if (p0 + r + 8 < P) sc_row[p0 + r + 8] = s1;
+            }
         }
         __syncwarp();  // the slot has been read by every lane
         if (a.tiles_done) {
@@ -854,11 +944,20 @@ cudaError_t launch_score_select(const ScoreSelectArgs& a, int num_sms, cudaStrea
     // keys, chosen and decision bit words, and (top-p) the page weights
     const size_t smem = ((size_t)a.max_pages + 2 * (((size_t)a.max_pages + 31) / 32) +
                          (a.pol.mode == SPD_BUDGET_TOP_P ? (size_t)a.max_pages : 0)) * sizeof(uint32_t);
-    e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     long long sgrid = (long long)a.B * a.H_kv;
-    if (a.tiles_done && sgrid > 2LL * num_sms) sgrid = 2LL * num_sms;
-    return launch_pdl(select_kernel, dim3((unsigned)sgrid), dim3(kSelThreads), smem, st, a);
+    if (a.tiles_done) {
+        // chained step: two 128-thread CTAs per SM, resident beside the scoring CTAs
+        // from the start (so the attention grid is launched early), rows in order
+        auto kern = select_kernel<kSelThreadsChained>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (sgrid > 2LL * num_sms) sgrid = 2LL * num_sms;
+        return launch_pdl(kern, dim3((unsigned)sgrid), dim3(kSelThreadsChained), smem, st, a);
+    }
+    auto kern = select_kernel<kSelThreads>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3((unsigned)sgrid), dim3(kSelThreads), smem, st, a);
 }
 
 }  // namespace spd

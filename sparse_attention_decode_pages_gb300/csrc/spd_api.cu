@@ -192,6 +192,10 @@ static size_t score_ws_prefix(const spd_dims* dims) {
     return align256(16 + (size_t)dims->B * dims->H_kv * sizeof(int));
 }
 
+// Bytes of attn_ws_layout the kernel touches: with one unit per row (S = 1) only
+// the queue and the tickets (no partials).
+size_t attn_ws_needed(long long rows, int S, int R, int D);
+
 AttnWs attn_ws_layout(void* ws, long long rows, int S, int R, int D) {
     AttnWs w;
     size_t off = 0;
@@ -206,6 +210,11 @@ AttnWs attn_ws_layout(void* ws, long long rows, int S, int R, int D) {
     off += (size_t)rows * S * R * D * sizeof(float);
     w.bytes = off;
     return w;
+}
+
+size_t attn_ws_needed(long long rows, int S, int R, int D) {
+    if (S == 1) return align256(16 + (size_t)rows * sizeof(int));
+    return attn_ws_layout(nullptr, rows, S, R, D).bytes;
 }
 
 }  // namespace
@@ -455,8 +464,8 @@ static spd_status attn_common(const spd_dims* dims, const spd_bf16* q, const spd
     return SPD_OK;
 }
 
-// Validates and launches the sparse attention kernel with S splits (S >= 1 already
-// chosen); sel_done != NULL chains it behind the selection of each row.
+// Validates and launches the sparse attention kernel with S units per row (S >= 1
+// already chosen); sel_done != NULL chains it behind the selection of each row.
 static spd_status sparse_attn_launch(const spd_dims* dims, const spd_bf16* q, const spd_bf16* K, const spd_bf16* V,
                                      const int32_t* page_table, const int32_t* seq_lens, const int32_t* sel,
                                      const int32_t* nsel, int32_t k_max, int S, float softmax_scale, spd_bf16* o,
@@ -466,7 +475,8 @@ static spd_status sparse_attn_launch(const spd_dims* dims, const spd_bf16* q, co
     const int G = dims->H_q / dims->H_kv;
     const long long rows = (long long)dims->B * dims->H_kv;
     AttnWs w = attn_ws_layout(ws, rows, S, G, dims->D);
-    if (!ws || ws_bytes < w.bytes) return fail(SPD_ERR_WORKSPACE, "workspace %zu bytes < %zu", ws_bytes, w.bytes);
+    const size_t need = attn_ws_needed(rows, S, G, dims->D);
+    if (!ws || ws_bytes < need) return fail(SPD_ERR_WORKSPACE, "workspace %zu bytes < %zu", ws_bytes, need);
     if (!aligned16(ws)) return fail(SPD_ERR_INVALID_ARG, "ws must be 16-byte aligned");
     CUtensorMap tk, tv;
     if ((st = kv_map(&tk, K, dims)) != SPD_OK || (st = kv_map(&tv, V, dims)) != SPD_OK) return st;
@@ -515,22 +525,23 @@ SPD_API spd_status sparse_decode_attn(const spd_dims* dims, const spd_bf16* q, c
     if (!sel || !nsel) return fail(SPD_ERR_INVALID_ARG, "NULL selection");
     DevInfo* d = dev_info(&st);
     if (!d) return st;
-    const int S = sparse_splits(dims, k_max, num_splits, d->sms);
-    return sparse_attn_launch(dims, q, K, V, page_table, seq_lens, sel, nsel, k_max, S, softmax_scale, o, lse, ws,
-                              ws_bytes, nullptr, d, stream);
+    return sparse_attn_launch(dims, q, K, V, page_table, seq_lens, sel, nsel, k_max,
+                              sparse_splits(dims, k_max, num_splits, d->sms), softmax_scale, o, lse, ws, ws_bytes,
+                              nullptr, d, stream);
 }
 
-// The chained step's workspace: [score / select][chain: tile counter, warps done,
-// tiles_done[rows], sel_done[rows]][attention].
+// The chained step's workspace: [score / select][chain: two tile counters, warps
+// done, tiles_done[rows], sel_done[rows], (256-aligned) keys[rows][max_pages]][attention].
 struct StepWs {
-    size_t score, chain, attn, bytes;
+    size_t score, chain, keys, attn, bytes;
 };
 
 static bool step_ws_layout(const spd_dims* dims, int32_t k_max, StepWs* w, DevInfo* d) {
     const long long rows = (long long)dims->B * dims->H_kv;
     const int S = sparse_splits(dims, k_max, 0, d->sms);
     w->score = align256(spd_score_select_workspace_size(dims));
-    w->chain = align256(16 + 2 * (size_t)rows * sizeof(unsigned));
+    w->keys = align256(32 + 2 * (size_t)rows * sizeof(unsigned));  // offset of the keys in the chain part
+    w->chain = w->keys + align256((size_t)rows * dims->max_pages_per_seq * sizeof(unsigned));
     w->attn = attn_ws_layout(nullptr, rows, S, dims->H_q / dims->H_kv, dims->D).bytes;
     w->bytes = w->score + w->chain + w->attn;
     return w->score != 0;
@@ -580,19 +591,17 @@ SPD_API spd_status sparse_decode_step(const spd_dims* dims, spd_bf16* K, spd_bf1
         a.v_new = v_new;
         a.summ_w = summ;
     }
-    // Chained when every row is one attention unit: the selection of a row starts as
-    // soon as its tiles are scored and its attention as soon as it is selected.
+    // Chained row by row: the selection of a row starts as soon as its tiles are
+    // scored, and each of its attention units as soon as it is selected.
     const int S = sparse_splits(dims, k_max, 0, d->sms);
-    unsigned* sel_done = nullptr;
-    if (S == 1) {
-        char* chain = base + w.score;
-        const long long rows = (long long)dims->B * dims->H_kv;
-        a.tile_ctr = reinterpret_cast<unsigned long long*>(chain);
-        a.warps_done = reinterpret_cast<unsigned*>(chain + 8);
-        a.tiles_done = reinterpret_cast<unsigned*>(chain + 16);
-        a.sel_done = a.tiles_done + rows;
-        sel_done = a.sel_done;
-    }
+    char* chain = base + w.score;
+    const long long rows = (long long)dims->B * dims->H_kv;
+    a.tile_ctr = reinterpret_cast<unsigned long long*>(chain);
+    a.warps_done = reinterpret_cast<unsigned*>(chain + 16);
+    a.tiles_done = reinterpret_cast<unsigned*>(chain + 32);
+    a.sel_done = a.tiles_done + rows;
+    a.keys = reinterpret_cast<unsigned*>(chain + w.keys);
+    unsigned* sel_done = a.sel_done;
     cudaError_t e = launch_score_select(a, d->sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sparse_decode_step scoring launch");
     return sparse_attn_launch(dims, q, K, V, page_table, seq_lens, sel, nsel, k_max, S, softmax_scale, o, lse,
@@ -719,50 +728,21 @@ SPD_API spd_status sparse_decode_attn_noalloc(const spd_dims* dims, const spd_bf
     const int G = dims->H_q / dims->H_kv;
     const long long rows = (long long)dims->B * dims->H_kv;
     int S = sparse_splits(dims, k_max, num_splits, d->sms);
-    AttnWs w = attn_ws_layout(scratch, rows, S, G, dims->D);
     if (num_splits == 0) {
-        // automatic: the largest split count up to the usual one whose partials fit
-        while (w.bytes > SPD_NOALLOC_SCRATCH_BYTES && S > 1) {
+        // automatic: the usual split count, or fewer until the partials fit
+        while (S > 1 && attn_ws_needed(rows, S, G, dims->D) > SPD_NOALLOC_SCRATCH_BYTES)
             S = sparse_splits(dims, k_max, S - 1, d->sms);
-            w = attn_ws_layout(scratch, rows, S, G, dims->D);
-        }
     }
-    if (w.bytes > SPD_NOALLOC_SCRATCH_BYTES)
+    const size_t need = attn_ws_needed(rows, S, G, dims->D);
+    if (need > SPD_NOALLOC_SCRATCH_BYTES)
         return fail(SPD_ERR_UNSUPPORTED,
                     "sparse_decode_attn_noalloc needs %zu bytes of scratch for %d split(s); the fixed array holds %zu",
-                    w.bytes, S, (size_t)SPD_NOALLOC_SCRATCH_BYTES);
-    CUtensorMap tk, tv;
-    if ((st = kv_map(&tk, K, dims)) != SPD_OK || (st = kv_map(&tv, V, dims)) != SPD_OK) return st;
+                    need, S, (size_t)SPD_NOALLOC_SCRATCH_BYTES);
     // the queue and the split tickets must start at zero
+    const AttnWs w = attn_ws_layout(scratch, rows, S, G, dims->D);
     const size_t zero_bytes = reinterpret_cast<char*>(w.part_lse) - static_cast<char*>(scratch);
     cudaError_t e = cudaMemsetAsync(scratch, 0, zero_bytes, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "clearing the fixed scratch array");
-    AttnArgs a{};
-    a.q = q;
-    a.page_table = page_table;
-    a.seq_lens = seq_lens;
-    a.sel = sel;
-    a.nsel = nsel;
-    a.k_max = k_max;
-    a.B = dims->B;
-    a.H_q = dims->H_q;
-    a.H_kv = dims->H_kv;
-    a.D = dims->D;
-    a.ps = dims->page_size;
-    a.max_pages = dims->max_pages_per_seq;
-    a.T = 1;
-    a.num_phys = dims->num_phys_pages;
-    a.items_per_split = (k_max + S - 1) / S;
-    a.num_splits = S;
-    a.scale_log2 = softmax_scale * kLog2e;
-    a.o = o;
-    a.lse = lse;
-    a.part_o = w.part_o;
-    a.part_lse = w.part_lse;
-    a.counters = w.counters;
-    a.queue = w.queue;
-    a.num_sms = d->sms;
-    a.status = d->status;
-    e = launch_sparse_attn(a, tk, tv, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? SPD_OK : cuda_fail(e, "sparse_decode_attn_noalloc launch");
+    return sparse_attn_launch(dims, q, K, V, page_table, seq_lens, sel, nsel, k_max, S, softmax_scale, o, lse,
+                              scratch, SPD_NOALLOC_SCRATCH_BYTES, nullptr, d, stream);
 }
