@@ -9,21 +9,33 @@ timed as one sparse_decode_step call (the three kernels chained row by row):
       summary of its page rebuilt (f1, by the scoring pass itself; the a1
       summaries of the rest of the cache are resident), upper-bound scores of
       every page and the top-k budget,
-  a5-a6  sparse_decode_attn (split-K over the selected pages, fused merge),
+  a5-a6  sparse attention over the selected pages (split-K where rows are few,
+      fused merge),
   a7  dense_verify_attn of k+1 = 7 drafted positions over the full cache.
 
 The headline metric is sparse decode-attention tokens/s (B tokens per pass of
-f1 and a2-a6); a7 is timed in the same steps and reported under "dense_verify".  Each
-kernel is timed with CUDA events on the launching stream; L2 is evicted between timed passes
-(a 512 MiB read, outside the events; a write flush would leave ~L2-size of
-dirty lines to be written back during the next timed kernel).  The KV cache and the
-page summaries are resident in HBM (they are the cache); e2e adds, per step,
-the host->device copy of the step's inputs (q, the new token's K / V,
-seq_lens, page_table), staged in one pinned buffer, to the
-device and the copy of o and lse back, one copy each way.
+f1 and a2-a6); `roofline` is that whole step against the measured HBM copy peak,
+over the bytes the method must move (selected K/V tokens, every page summary,
+q / o / lse, and the append).  a7 is timed in the same steps (`dense_verify`).
+Each kernel is timed with CUDA events on the launching stream; L2 is evicted
+between timed passes (a 512 MiB read, outside the events; a write flush would
+leave ~L2-size of dirty lines to be written back during the next timed kernel).
+The KV cache and the page summaries are resident in HBM (they are the cache);
+e2e adds, per step, the host->device copy of the step's inputs (q, the new
+token's K / V, seq_lens, page_table), staged in one pinned buffer, and the copy
+of o and lse back, one copy each way.
+
+`configs` measures every workload shape of the sweep the same way (tiny, the
+Qwen3-1.7B shape with planted retrieval tokens, the Qwen3-8B shape, the
+page-size sweep at 16 / 32 / 64, the long-tail batch with split-K), the dense
+T = 1 decode beside the tiny and long-tail ones, the retrieval recall of the
+selection where tokens are planted, a parity check of sampled sequences against
+the fp64 oracle and the oracle's own time on those sequences.
 
 --impl reference times the fp64 CPU oracle (there is no other reference
 implementation of this path) on the same workload and metric.
+--gpus N without a launcher re-runs this script under torch.distributed.run with
+N processes (independent replicas, one per GPU).
 """
 from __future__ import annotations
 
@@ -32,6 +44,7 @@ import hashlib
 import json
 import math
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -47,17 +60,36 @@ from sparse_attention_decode_pages_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "sparse decode-attn tokens/s and HBM GB/s (% of roofline), Qwen3-8B shape"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
 L2_FLUSH_BYTES = 512 << 20  # read between timed passes: evicts L2 (129 MB) and leaves it clean
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = ["common.cuh", "kernels.h", "attn.cuh", "attn_sparse.cu"]  # the sparse attention kernel
+CSRC = os.path.join(ROOT, "sparse_attention_decode_pages_gb300", "csrc")
+# sources of the kernels whose DRAM traffic profiles/traffic.json records
+ATTN_SOURCES = ["common.cuh", "kernels.h", "attn.cuh", "attn_sparse.cu"]
+STEP_SOURCES = ["common.cuh", "kernels.h", "attn.cuh", "attn_sparse.cu", "score_select.cu", "spd_api.cu"]
+# the workloads of the sweep: (name, page size, dense T = 1 decode beside the sparse step)
+CONFIGS = [("tiny", None, True), ("q17b", None, False), ("q8b", None, False), ("sweep", 16, False),
+           ("sweep", 32, False), ("sweep", 64, False), ("longtail", None, True)]
 
 
-def kernel_source_hash() -> str:
+def source_hash(files) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "sparse_attention_decode_pages_gb300", "csrc", f), "rb") as fh:
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def recorded_traffic(key, files):
+    """DRAM bytes per launch recorded by an ncu capture, if the sources are unchanged since."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            ent = json.load(fh).get(key)
+        if ent and ent.get("source_hash") == source_hash(files):
+            return ent["bytes_per_launch"]
+    except Exception:
+        pass
+    return None
 
 
 def staged(torch, dev, tensors):
@@ -107,33 +139,39 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def algorithmic_bytes(w, nsel):
-    """Bytes the method must move per pass (valid tokens of selected pages, summaries, q/o/lse)."""
+def algorithmic_bytes(w, chosen):
+    """Bytes the method must move per pass: the valid tokens of the selected pages
+    (K and V), every page summary, q / o / lse, and the append (the new token's K
+    and V read and written, the older tokens of its page read, its summary written)."""
     ps, D, H_kv = w.page_size, w.D, w.H_kv
-    kv = 0
-    summ = 0
+    kv = summ = refresh = 0
     for b in range(w.B):
         L = int(w.seq_lens[b])
-        P = w.pages(b)
-        summ += P * H_kv * 4 * D
+        summ += w.pages(b) * H_kv * 4 * D
         for h in range(H_kv):
-            pages = nsel[b][h]
-            toks = sum(min(ps, L - p * ps) for p in pages)
-            kv += toks * 4 * D
-    qo = w.B * w.H_q * D * 2 * 2 + w.B * w.H_q * 4
-    # f1: the new token's K and V written, the older tokens of its page read, the
-    # page summary written
-    refresh = 0
-    for b in range(w.B):
-        L = int(w.seq_lens[b])
+            kv += sum(min(ps, L - p * ps) for p in chosen[b][h]) * 4 * D
         old = (L - 1) - ((L - 1) // ps) * ps
-        refresh += H_kv * (2 * D * 2 + old * D * 2 + 4 * D) + H_kv * 2 * D * 2  # + k_new/v_new read
-    return dict(attn=kv + qo, score=summ + w.B * w.H_q * D * 2, refresh=refresh,
-                step=kv + summ + qo + refresh)
+        refresh += H_kv * (2 * D * 2 + old * D * 2 + 4 * D) + H_kv * 2 * D * 2
+    qo = w.B * w.H_q * D * 2 * 2 + w.B * w.H_q * 4
+    return dict(selected_kv=kv, summaries=summ, q_o_lse=qo, append=refresh,
+                attn=kv + qo, score=summ + w.B * w.H_q * D * 2, step=kv + summ + qo + refresh)
 
 
 def verify_bytes(w, T):
     return sum(int(w.seq_lens[b]) * w.H_kv * 4 * w.D for b in range(w.B)) + w.B * T * w.H_q * w.D * 4
+
+
+def retrieval_recall(w, sel, nsel):
+    """Fraction of the planted retrieval tokens whose page the selection of their
+    (sequence, KV head) keeps (every KV head gets the aligned key), or None."""
+    hit = tot = 0
+    for b in range(w.B):
+        for pos in w.planted[b]:
+            p = pos // w.page_size
+            for h in range(w.H_kv):
+                tot += 1
+                hit += int(p in set(sel[b, h, : nsel[b, h]].tolist()))
+    return None if tot == 0 else hit / tot
 
 
 class ClockSampler:
@@ -193,6 +231,143 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def _timed(torch, stream, flush, fn, reps, warmup):
+    """Median device time (ms) of fn() between events on the stream, L2 evicted before each."""
+    for _ in range(warmup):
+        fn()
+    out = []
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        out.append(a.elapsed_time(b))
+    return float(np.median(out))
+
+
+class Case:
+    """One workload on the device: its cache, summaries, the step's new token (the K / V
+    already at position len - 1, so every pass rewrites the same values and the cache
+    stays the same workload), outputs and workspaces."""
+
+    def __init__(self, spd, torch, dev, w):
+        self.spd, self.torch, self.dev, self.w = spd, torch, dev, w
+        d = self.d = wl.to_device(w, dev)
+        self.dims = spd.dims_of(w.B, w.H_q, w.H_kv, w.D, w.page_size, w.max_pages_per_seq, w.num_phys_pages)
+        self.summ = torch.empty((w.B, w.H_kv, w.max_pages_per_seq, 2, w.D), dtype=torch.bfloat16, device=dev)
+        spd.pages_summarize(self.dims, d["K"], d["page_table"], d["seq_lens"], self.summ)  # prefill
+        lens = w.seq_lens.astype(np.int64)
+        ph = torch.from_numpy(w.page_table[np.arange(w.B), (lens - 1) // w.page_size].astype(np.int64)).to(dev)
+        slot = torch.from_numpy((lens - 1) % w.page_size).to(dev)
+        self.k_new = d["K"][ph, :, slot].unsqueeze(1).contiguous()  # [B][1][H_kv][D]
+        self.v_new = d["V"][ph, :, slot].unsqueeze(1).contiguous()
+        self.sel = torch.empty((w.B, w.H_kv, w.k_max), dtype=torch.int32, device=dev)
+        self.nsel = torch.empty((w.B, w.H_kv), dtype=torch.int32, device=dev)
+        self.o = torch.empty((w.B, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((w.B, w.H_q), dtype=torch.float32, device=dev)
+        self.policy = spd.policy_of(w.policy)
+        self.ws_step = spd.workspace(spd.spd_sparse_decode_step_workspace_size(self.dims, w.k_max), dev)
+
+    def step(self):
+        """One sparse decode step in one call: append, score + select, attention."""
+        d = self.d
+        self.spd.sparse_decode_step(self.dims, d["K"], d["V"], d["page_table"], d["seq_lens"], self.k_new,
+                                    self.v_new, d["q"], self.summ, self.policy, self.sel, self.nsel,
+                                    self.w.k_max, self.o, self.ws_step, lse=self.lse)
+
+    def chosen(self):
+        n, s = self.nsel.cpu().numpy(), self.sel.cpu().numpy()
+        return [[s[b, h, : n[b, h]].tolist() for h in range(self.w.H_kv)] for b in range(self.w.B)], s, n
+
+
+def _sample(w, k=2):
+    """Sequences checked against (and timed with) the oracle: the first and the last."""
+    return sorted({0, w.B - 1})[:k]
+
+
+def oracle_sample(w, sel, nsel, o, lse, dense=None):
+    """Parity of sampled sequences against the fp64 oracle, and the oracle's time on them.
+
+    Selection: the share of sampled (sequence, KV head) rows whose page set equals the
+    oracle's.  Attention: the oracle over the GPU's own selection (so the numbers
+    measure the attention arithmetic, not a tie in the selection).  The CPU time is
+    scores + selection + sparse attention of the sampled sequences, one thread each,
+    summaries precomputed."""
+    import oracle
+    seqs = _sample(w)
+    n = len(seqs)
+    summ = oracle.summarize(w, seqs=seqs, threads=n)
+    t0 = time.perf_counter()
+    sc = oracle.scores(w, summ, seqs=seqs, threads=n)
+    sel_r, nsel_r = oracle.select(w, sc, seqs=seqs, threads=n)
+    o_r, lse_r = oracle.sparse_attn(w, sel_r, nsel_r, seqs=seqs, threads=n)
+    el = time.perf_counter() - t0
+    same = sum(int(nsel[b, h] == nsel_r[b, h] and np.array_equal(sel[b, h, : nsel[b, h]], sel_r[b, h, : nsel_r[b, h]]))
+               for b in seqs for h in range(w.H_kv))
+    o_g, lse_g = oracle.sparse_attn(w, sel, nsel, seqs=seqs, threads=n)
+    err = np.abs(o[seqs].astype(np.float64) - o_g[seqs])
+    res = {"sequences": seqs, "selection_rows_identical": same / (n * w.H_kv),
+           "o_max_abs": float(err.max()), "o_mean_abs": float(err.mean()),
+           "lse_max_abs": float(np.max(np.abs(lse[seqs] - lse_g[seqs]))),
+           "cpu_baseline": {"value": n / el, "unit": "tokens/s", "cores": n, "kind": "oracle",
+                            "sample": f"scores + selection + sparse attention of sequences {seqs}"}}
+    if dense is not None:
+        o_d, lse_d = dense
+        q1 = np.ascontiguousarray(w.q.reshape(w.B, 1, w.H_q, w.D))
+        t0 = time.perf_counter()
+        ov_r, lv_r = oracle.verify(w, 1, q=q1, seqs=seqs, threads=n)
+        el = time.perf_counter() - t0
+        e = np.abs(o_d[seqs].astype(np.float64) - ov_r[seqs, 0])
+        res["dense_t1"] = {"o_max_abs": float(e.max()), "o_mean_abs": float(e.mean()),
+                           "lse_max_abs": float(np.max(np.abs(lse_d[seqs] - lv_r[seqs, 0]))),
+                           "cpu_baseline": {"value": n / el, "unit": "tokens/s", "cores": n, "kind": "oracle",
+                                            "sample": f"dense attention of sequences {seqs}"}}
+    return res
+
+
+def measure_config(spd, torch, dev, name, ps, dense, flush, peak, reps, warmup, stream):
+    """The sparse step (and the dense T = 1 decode) of one workload of the sweep."""
+    w = wl.named(name, ps)
+    c = Case(spd, torch, dev, w)
+    ms = _timed(torch, stream, flush, c.step, reps, warmup)
+    torch.cuda.synchronize()
+    if spd.spd_device_status(clear=True):
+        raise RuntimeError(f"device status set in the {name} sweep")
+    chosen, sel, nsel = c.chosen()
+    nb = algorithmic_bytes(w, chosen)
+    gbs = nb["step"] / (ms * 1e-3) / 1e9
+    res = {"name": name if ps is None else f"{name} ps{ps}",
+           "workload": f"B={w.B}, Hq/Hkv={w.H_q}/{w.H_kv}, D={w.D}, ps={w.page_size}, "
+                       f"len {int(w.seq_lens.min())}..{int(w.seq_lens.max())}, budget {w.policy.mode}"
+                       f" (mean {float(nsel.mean()):.1f} pages), sink {w.policy.sink_pages} + local "
+                       f"{w.policy.local_pages}",
+           "sparse_step": {"us": ms * 1e3, "tokens_per_s": w.B / (ms * 1e-3), "gb_s": gbs, "frac": gbs / peak,
+                           "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS, "bytes": nb["step"],
+                           "summary_share": nb["summaries"] / nb["step"]},
+           "recall_planted": retrieval_recall(w, sel, nsel)}
+    o_h, lse_h = c.o.float().cpu().numpy(), c.lse.cpu().numpy()
+    dense_out = None
+    if dense:
+        ov = torch.empty((w.B, 1, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
+        lv = torch.empty((w.B, 1, w.H_q), dtype=torch.float32, device=dev)
+        q1 = c.d["q"].view(w.B, 1, w.H_q, w.D)
+        wsv = spd.workspace(spd.spd_dense_verify_workspace_size(c.dims, 1, 0), dev)
+        msd = _timed(torch, stream, flush, lambda: spd.dense_verify_attn(
+            c.dims, 1, q1, c.d["K"], c.d["V"], c.d["page_table"], c.d["seq_lens"], ov, wsv, lse=lv), reps, warmup)
+        vb = verify_bytes(w, 1)
+        res["dense_t1"] = {"us": msd * 1e3, "tokens_per_s": w.B / (msd * 1e-3), "gb_s": vb / (msd * 1e-3) / 1e9,
+                           "frac": vb / (msd * 1e-3) / 1e9 / peak, "bytes": vb}
+        dense_out = (ov[:, 0].float().cpu().numpy(), lv[:, 0].cpu().numpy())
+    if spd.spd_device_status(clear=True):
+        raise RuntimeError(f"device status set in the {name} sweep")
+    res["oracle"] = oracle_sample(w, sel, nsel, o_h, lse_h, dense_out)
+    del c
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -216,28 +391,12 @@ def run_gpu(args):
     if w.q_verify is None:
         rng = np.random.default_rng(spec.seed + 7)
         w.q_verify = wl.f32_to_bf16_bits(rng.standard_normal((w.B, T, w.H_q, w.D)).astype(np.float32))
-    d = wl.to_device(w, dev)
-    dims = spd.dims_of(w.B, w.H_q, w.H_kv, w.D, w.page_size, w.max_pages_per_seq, w.num_phys_pages)
-    summ = torch.empty((w.B, w.H_kv, w.max_pages_per_seq, 2, w.D), dtype=torch.bfloat16, device=dev)
-    spd.pages_summarize(dims, d["K"], d["page_table"], d["seq_lens"], summ)  # prefill
-    # the step's new token: its K / V are the ones already at position len - 1, so
-    # every pass writes the same values and the cache stays the same workload
-    k_new = torch.empty((w.B, 1, w.H_kv, w.D), dtype=torch.bfloat16, device=dev)
-    v_new = torch.empty_like(k_new)
-    for b in range(w.B):
-        L = int(w.seq_lens[b])
-        ph = int(w.page_table[b, (L - 1) // w.page_size])
-        k_new[b, 0] = d["K"][ph, :, (L - 1) % w.page_size]
-        v_new[b, 0] = d["V"][ph, :, (L - 1) % w.page_size]
-    k_max = w.k_max
-    sel = torch.empty((w.B, w.H_kv, k_max), dtype=torch.int32, device=dev)
-    nsel = torch.empty((w.B, w.H_kv), dtype=torch.int32, device=dev)
-    o = torch.empty((w.B, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((w.B, w.H_q), dtype=torch.float32, device=dev)
+    c = Case(spd, torch, dev, w)
+    d, dims, summ, k_max = c.d, c.dims, c.summ, w.k_max
     # the step's inputs and outputs each in one device buffer (one copy each way in e2e)
-    inp_d, (d["q"], d["seq_lens"], d["page_table"], k_new, v_new) = staged(
-        torch, dev, [d["q"], d["seq_lens"], d["page_table"], k_new, v_new])
-    out_d, (o, lse) = staged(torch, dev, [o, lse])
+    inp_d, (d["q"], d["seq_lens"], d["page_table"], c.k_new, c.v_new) = staged(
+        torch, dev, [d["q"], d["seq_lens"], d["page_table"], c.k_new, c.v_new])
+    out_d, (c.o, c.lse) = staged(torch, dev, [c.o, c.lse])
     ov = torch.empty((w.B, T, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
     lsev = torch.empty((w.B, T, w.H_q), dtype=torch.float32, device=dev)
     ws_sel = spd.workspace(spd.spd_score_select_workspace_size(dims), dev)
@@ -245,36 +404,27 @@ def run_gpu(args):
     ws_ver = spd.workspace(spd.spd_dense_verify_workspace_size(dims, T, args.vsplits), dev)
     flush_buf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    class _Flush:
+    def flush():
         """Evicts L2 by reading a buffer 4x its size (a write would leave dirty lines
         to be written back during the next timed kernel)."""
+        flush_buf.sum()
 
-        @staticmethod
-        def zero_():
-            flush_buf.sum()
-
-    flush = _Flush()
     stream = torch.cuda.current_stream(dev)
-    policy = spd.policy_of(w.policy)
-
-    ws_step = spd.workspace(spd.spd_sparse_decode_step_workspace_size(dims, k_max), dev)
 
     def sparse_pass(ev=None):
         if ev is None and args.splits == 0:
-            # the whole step in one call: append, score + select and attention chained row by row
-            spd.sparse_decode_step(dims, d["K"], d["V"], d["page_table"], d["seq_lens"], k_new, v_new, d["q"],
-                                   summ, policy, sel, nsel, k_max, o, ws_step, lse=lse)
+            c.step()  # the whole step in one call: append, score + select and attention chained
             return
         if ev:
             ev[0].record(stream)
         # f1 + a2-a4: the step's token appended (its page's summary rebuilt) by the
         # scoring pass itself, then the selection
-        spd.pages_append_score_select(dims, d["K"], d["V"], d["page_table"], d["seq_lens"], k_new, v_new,
-                                      d["q"], summ, policy, sel, nsel, k_max, ws_sel)
+        spd.pages_append_score_select(dims, d["K"], d["V"], d["page_table"], d["seq_lens"], c.k_new, c.v_new,
+                                      d["q"], summ, c.policy, c.sel, c.nsel, k_max, ws_sel)
         if ev:
             ev[2].record(stream)
-        spd.sparse_decode_attn(dims, d["q"], d["K"], d["V"], d["page_table"], d["seq_lens"], sel,
-                               nsel, k_max, o, ws_attn, lse=lse, num_splits=args.splits)
+        spd.sparse_decode_attn(dims, d["q"], d["K"], d["V"], d["page_table"], d["seq_lens"], c.sel,
+                               c.nsel, k_max, c.o, ws_attn, lse=c.lse, num_splits=args.splits)
         if ev:
             ev[3].record(stream)
 
@@ -288,24 +438,23 @@ def run_gpu(args):
 
     for _ in range(args.warmup):
         sparse_pass()
-        flush.zero_()
+        flush()
         verify_pass()
-        flush.zero_()
+        flush()
     torch.cuda.synchronize()
     status = spd.spd_device_status(clear=True)
     if status:
         raise RuntimeError(f"device status {status:#x} after warm-up")
 
-    nsel_host = nsel.cpu().numpy()
-    sel_host = sel.cpu().numpy()
-    chosen = [[sel_host[b, h, : nsel_host[b, h]].tolist() for h in range(w.H_kv)] for b in range(w.B)]
+    chosen, sel_host, nsel_host = c.chosen()
+    o_host, lse_host = c.o.float().cpu().numpy(), c.lse.cpu().numpy()
     nbytes = algorithmic_bytes(w, chosen)
     vbytes = verify_bytes(w, T)
 
     # Two passes over the same K steps.  Pass A times each step as a whole (events
     # only at its ends, so the step's kernels overlap their launches as they do
     # in use); pass B puts events between the kernels (which serialises them)
-    # for the per-kernel breakdown and the attention kernel's roofline.
+    # for the per-kernel breakdown.
     sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     evs = [[torch.cuda.Event(enable_timing=True) if k != 1 else None for k in range(4)] for _ in range(args.steps)]
     vevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
@@ -317,14 +466,14 @@ def run_gpu(args):
     torch.cuda.synchronize()
     t0 = time.time()
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         sevs[i][0].record(stream)
         sparse_pass()
         sevs[i][1].record(stream)
-        flush.zero_()
+        flush()
         verify_pass(vevs[i])
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         sparse_pass(evs[i])
     torch.cuda.synchronize()
     if world > 1:
@@ -343,6 +492,7 @@ def run_gpu(args):
     ms_step = float(np.mean(t_step))
     ms_ver = float(np.mean(t_ver))
     ms_att = float(np.mean(t_att))
+    ms_sel = float(np.mean(t_sel))
 
     # e2e: the same sparse pass through the C ABI with host buffers: the step's inputs
     # (q, seq_lens, page_table, the new token's K / V) staged in one pinned buffer and
@@ -351,7 +501,7 @@ def run_gpu(args):
     out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
     e2e_ms = []
     for i in range(args.warmup + args.steps):
-        flush.zero_()
+        flush()
         ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ea.record(stream)
         inp_d.copy_(inp_h, non_blocking=True)
@@ -368,21 +518,36 @@ def run_gpu(args):
                                               reps=max(10, min(args.steps, 50)), warmup=args.warmup)
 
     # max over ranks
-    ms_step, ms_ver, ms_e2e, ms_att = max_over_ranks([ms_step, ms_ver, float(np.mean(e2e_ms)), ms_att], world, dev)
+    ms_step, ms_ver, ms_e2e, ms_att, ms_sel = max_over_ranks(
+        [ms_step, ms_ver, float(np.mean(e2e_ms)), ms_att, ms_sel], world, dev)
 
     peak, peak_src = hbm_peak()
-    att_gbs = nbytes["attn"] / (ms_att * 1e-3) / 1e9
+    peak_note = (f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, copy peak)" if peak_src == "measured"
+                 else "fallback 6.8 TB/s")
     step_gbs = nbytes["step"] / (ms_step * 1e-3) / 1e9
+    att_gbs = nbytes["attn"] / (ms_att * 1e-3) / 1e9
+    sel_gbs = (nbytes["score"] + nbytes["append"]) / (ms_sel * 1e-3) / 1e9
     ver_gbs = vbytes / (ms_ver * 1e-3) / 1e9
-    traffic = None
-    try:
-        with open(TRAFFIC_FILE) as fh:
-            tr = json.load(fh)
-        ent = tr.get(f"sparse_decode_attn/{args.config}")
-        if ent and ent.get("source_hash") == kernel_source_hash():
-            traffic = ent["bytes_per_launch"]
-    except Exception:
-        pass
+
+    configs = None
+    if rank == 0 and world == 1 and not args.no_configs:
+        configs = []
+        for name, ps, dense in CONFIGS:
+            if name == args.config and ps == args.page_size:
+                # the headline workload, measured above; its oracle sample here
+                configs.append({"name": name, "workload": "the headline workload (config)",
+                                "sparse_step": {"us": ms_step * 1e3, "tokens_per_s": w.B / (ms_step * 1e-3),
+                                                "gb_s": step_gbs, "frac": step_gbs / peak,
+                                                "frac_of_nominal_8tbs": step_gbs / NOMINAL_HBM_GBS,
+                                                "bytes": nbytes["step"],
+                                                "summary_share": nbytes["summaries"] / nbytes["step"]},
+                                "dense_verify_t7": {"us": ms_ver * 1e3, "tokens_per_s": w.B * T / (ms_ver * 1e-3),
+                                                    "gb_s": ver_gbs, "frac": ver_gbs / peak},
+                                "recall_planted": retrieval_recall(w, sel_host, nsel_host),
+                                "oracle": oracle_sample(w, sel_host, nsel_host, o_host, lse_host)})
+                continue
+            configs.append(measure_config(spd, torch, dev, name, ps, dense, flush, peak, reps=20,
+                                          warmup=3, stream=stream))
 
     if rank == 0:
         cpu = None
@@ -409,22 +574,32 @@ def run_gpu(args):
                 "global_batch": world * w.B,
                 "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                 "l2": "evicted between timed passes by reading a 512 MiB buffer (outside the events)",
-                "timing": "value from whole-step events around sparse_decode_step (its kernels chained row by "
-                          "row); the per-kernel breakdown and the roofline from a second pass of the separate "
+                "timing": "value and roofline from whole-step events around sparse_decode_step (its kernels "
+                          "chained row by row); the per-kernel breakdown from a second pass of the separate "
                           "calls with events between them",
                 "splits": args.splits, "verify_splits": args.vsplits,
             },
+            # the gated quantity: score + select + sparse attention + merge (with the step's
+            # append), over the bytes the method must move
+            "roofline": {"bound": "hbm", "kernel": "sparse_decode_step (append + score + select + sparse "
+                                                  "attention + merge, chained)",
+                         "achieved": step_gbs, "peak": peak, "unit": "GB/s", "frac": step_gbs / peak,
+                         "frac_of_nominal_8tbs": step_gbs / NOMINAL_HBM_GBS,
+                         "traffic": recorded_traffic(f"sparse_decode_step/{args.config}", STEP_SOURCES),
+                         "algorithmic_bytes": nbytes["step"],
+                         "bytes": {k: nbytes[k] for k in ("selected_kv", "summaries", "q_o_lse", "append")},
+                         "peak_source": peak_note},
+            "kernels": {
+                "sparse_attn": {"kernel": "attn_kernel (sparse, fused merge), separate call", "ms": ms_att,
+                                "achieved": att_gbs, "frac": att_gbs / peak, "unit": "GB/s",
+                                "algorithmic_bytes": nbytes["attn"],
+                                "traffic": recorded_traffic(f"sparse_decode_attn/{args.config}", ATTN_SOURCES)},
+                "append_score_select": {"kernel": "score_select_kernel + select_kernel, separate call",
+                                        "ms": ms_sel, "achieved": sel_gbs, "frac": sel_gbs / peak,
+                                        "unit": "GB/s", "algorithmic_bytes": nbytes["score"] + nbytes["append"]},
+            },
             "step_ms": {"whole_step": ms_step, "serialised_step": float(np.mean(t_step_serial)),
-                        "f1_a2_a4_append_score_select": float(np.mean(t_sel)),
-                        "a5_a6_sparse_attn": ms_att},
-            "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s",
-                              "frac": step_gbs / peak, "bytes": nbytes["step"],
-                              "frac_of_nominal_8tbs": step_gbs / 8000.0},
-            "roofline": {"bound": "hbm", "kernel": "sparse_decode_attn", "achieved": att_gbs,
-                         "peak": peak, "unit": "GB/s", "frac": att_gbs / peak,
-                         "traffic": traffic, "algorithmic_bytes": nbytes["attn"],
-                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
-                         if peak_src == "measured" else "fallback 6.8 TB/s"},
+                        "f1_a2_a4_append_score_select": ms_sel, "a5_a6_sparse_attn": ms_att},
             "dense_verify": {"tokens_per_s": world * w.B * T / (ms_ver * 1e-3), "ms": ms_ver,
                              "achieved_gbs": ver_gbs, "frac": ver_gbs / peak, "bytes": vbytes,
                              "tflops": 4.0 * sum(int(w.seq_lens[b]) for b in range(w.B)) * w.H_q * T * w.D
@@ -437,27 +612,12 @@ def run_gpu(args):
             "clocks": clocks,
             "wall_s_timed_region": t1 - t0,
             "cpu_baseline": cpu,
+            "configs": configs,
             "next_rows": nxt,
         }
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
-
-
-def _timed(torch, stream, flush, fn, reps, warmup):
-    """Median device time (ms) of fn() between events on the stream, L2 evicted before each."""
-    for _ in range(warmup):
-        fn()
-    out = []
-    for _ in range(reps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        fn()
-        b.record(stream)
-        b.synchronize()
-        out.append(a.elapsed_time(b))
-    return float(np.median(out))
 
 
 def next_rows(spd, torch, w, d, dims, summ, stream, flush, peak_of, reps, warmup):
@@ -609,9 +769,22 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def replica_launch_cmd(argv, n, port):
+    """The command that runs this benchmark as n independent replicas, one process per GPU."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1, help="replicas (one per GPU); without a launcher the "
+                                                        "script re-runs itself under torch.distributed.run")
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -621,10 +794,16 @@ def main():
     ap.add_argument("--vsplits", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip the measurements of the rows after the core path")
+    ap.add_argument("--no-configs", action="store_true", help="skip the sweep over the other workload shapes")
     ap.add_argument("--batch", type=int, default=0, help="override B (small profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    world = os.environ.get("WORLD_SIZE")
+    if args.gpus > 1 and world is None:
+        sys.exit(subprocess.call(replica_launch_cmd(sys.argv[1:], args.gpus, _free_port())))
+    if world is not None and int(world) != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; running {world} replicas", file=sys.stderr)
     if args.impl == "reference":
         run_reference(args)
     else:

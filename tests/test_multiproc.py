@@ -89,3 +89,48 @@ def test_staged_inputs_are_views_of_one_buffer():
         assert (v.data_ptr() - base) % 256 == 0
     views[0].fill_(7)  # a view: writes land in the buffer
     assert torch.equal(buf[:40].view(torch.int32), torch.full((10,), 7, dtype=torch.int32))
+
+
+def test_gpus_flag_runs_replicas_under_a_launcher():
+    """`bench.py --gpus 2` without a launcher re-runs itself under torch.distributed.run
+    with two processes: here the reference arm, so rank 0 alone prints one line."""
+    import json
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--impl", "reference",
+                        "--steps", "1", "--warmup", "3", "--config", "tiny"], env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-800:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    assert json.loads(lines[0])["n_gpus"] == 2
+
+
+def test_replica_launch_command():
+    import bench
+    cmd = bench.replica_launch_cmd(["--gpus", "4", "--steps", "3"], 4, 12345)
+    assert cmd[1:4] == ["-m", "torch.distributed.run", "--nnodes=1"] and "--nproc-per-node=4" in cmd
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1" and cmd[cmd.index("--master-port") + 1] == "12345"
+    assert cmd[-4:] == ["--gpus", "4", "--steps", "3"]
+
+
+def test_retrieval_recall_and_byte_breakdown():
+    """Recall counts, per KV head, the planted tokens whose page is selected; the step's
+    algorithmic bytes are the sum of their parts, with a summary read per page."""
+    import bench
+    from sparse_attention_decode_pages_gb300 import workloads as wl
+    w = wl.named("q17b", B=2, len_lo=600, len_hi=900, threads=2)
+    assert all(len(p) == 8 for p in w.planted)
+    ps = w.page_size
+    sel = np.full((w.B, w.H_kv, 4), -1, np.int32)
+    nsel = np.zeros((w.B, w.H_kv), np.int32)
+    pos = w.planted[0][0] // ps
+    sel[0, :, 0] = pos                       # every head of sequence 0 keeps one planted page
+    nsel[0, :] = 1
+    want = sum(1 for t in w.planted[0] if t // ps == pos) * w.H_kv / (8 * w.B * w.H_kv)
+    assert bench.retrieval_recall(w, sel, nsel) == pytest.approx(want)
+    chosen = [[[0, w.pages(b) - 1] for _ in range(w.H_kv)] for b in range(w.B)]
+    nb = bench.algorithmic_bytes(w, chosen)
+    assert nb["step"] == nb["selected_kv"] + nb["summaries"] + nb["q_o_lse"] + nb["append"]
+    assert nb["summaries"] == sum(w.pages(b) for b in range(w.B)) * w.H_kv * 4 * w.D
+    full_last = [min(ps, int(w.seq_lens[b]) - (w.pages(b) - 1) * ps) for b in range(w.B)]
+    assert nb["selected_kv"] == sum((ps + full_last[b]) * w.H_kv * 4 * w.D for b in range(w.B))
