@@ -372,41 +372,27 @@ void oracle_append_seq(int T, int H_kv, int D, int ps, int max_pages, uint16_t *
 }
 
 /*
- * Weight of a probability in the draw: floor(2^40 * v), exactly (scaling a
- * float by a power of two is exact and the conversion truncates).  Values at
- * or above 1 count as 1; zero, negative and NaN values count as 0.
+ * A draw with a uniform u in [0, 1) from non-negative weights w[0..n): the
+ * smallest x whose running sum (in index order) exceeds u * sum(w) -- inverting
+ * the cumulative distribution.  The last running sum is the total itself (the
+ * same additions in the same order), which exceeds u * total for u < 1.  All
+ * weights zero: -1.
  */
-static uint64_t fixed40(float v)
+static int draw(const double *w, int n, double u)
 {
-    if (!(v > 0.0f)) return 0;
-    if (v >= 1.0f) return (uint64_t)1 << 40;
-    return (uint64_t)(v * 0x1p40f);
+    double total = 0.0;
+    for (int x = 0; x < n; ++x) total += w[x];
+    if (!(total > 0.0)) return -1;
+    double t = u * total, run = 0.0;
+    for (int x = 0; x < n; ++x) {
+        run += w[x];
+        if (run > t) return x;
+    }
+    return -1; /* not reached */
 }
 
-/*
- * A draw from integer weights W[0..n) with a uniform float u in [0, 1): the
- * smallest x whose running sum exceeds T = floor(u * sum(W)), all in exact
- * integer arithmetic (u = m * 2^e with an integer m; the product m * sum(W)
- * needs 128 bits).  All weights zero: -1.
- */
-static int draw_fixed(const uint64_t *W, int n, float u)
-{
-    uint64_t total = 0;
-    for (int x = 0; x < n; ++x) total += W[x];
-    if (total == 0) return -1;
-    int e;
-    double fr = frexp((double)u, &e);           /* u = fr * 2^e, fr in [0.5, 1) */
-    uint64_t m = (uint64_t)ldexp(fr, 24);       /* exact: u has 24 significant bits */
-    int shift = 24 - e;                         /* u = m * 2^-shift */
-    unsigned __int128 prod = (unsigned __int128)m * total;
-    uint64_t target = shift >= 128 ? 0 : (uint64_t)(prod >> shift);
-    uint64_t run = 0;
-    for (int x = 0; x < n; ++x) {
-        run += W[x];
-        if (run > target) return x;
-    }
-    return -1; /* not reached: target < total for u < 1 */
-}
+/* A probability as a weight: negative and NaN values weigh nothing. */
+static double weight(double v) { return v > 0.0 ? v : 0.0; }
 
 /*
  * Row f2 -- exact speculative sampling (the S3R abstract: responses come from
@@ -419,11 +405,7 @@ static int draw_fixed(const uint64_t *W, int n, float u)
  *   at the first rejection j, emit a draw (u_res) from the residual
  *   max(0, q_j - p_j), or from q_j when the residual is zero everywhere;
  *   if all k drafts are accepted, emit a bonus draw (u_res) from q_k.
- * The draw's weights are probabilities on a grid of 2^-40, so that every sum
- * is exact and independent of order: the residual weight of x is
- * max(0, floor(2^40 q(x)) - floor(2^40 p(x))), the plain weight
- * floor(2^40 q(x)).  (Tokens below 2^-40 of mass are never drawn: a total
- * variation of at most n * 2^-40 from the exact rule.)
+ * The draws are plain inverse-CDF draws in double precision.
  * p is [k][n] and q is [k+1][n] fp32.  tokens[0..k] receives the accepted
  * drafts then the emitted token, -1 after it; the return value is the number
  * of accepted drafts.
@@ -439,22 +421,19 @@ int oracle_spec_accept_seq(int k, int n, const float *p, const float *q, const i
         tokens[acc] = x;
         ++acc;
     }
-    uint64_t *W = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(n > 0 ? n : 1));
+    double *w = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
     const float *qr = q + (size_t)acc * n;
     int tok = -1;
     if (acc < k) {
         const float *pr = p + (size_t)acc * n;
-        for (int x = 0; x < n; ++x) {
-            uint64_t a = fixed40(qr[x]), b = fixed40(pr[x]);
-            W[x] = a > b ? a - b : 0;
-        }
-        tok = draw_fixed(W, n, u_res);
+        for (int x = 0; x < n; ++x) w[x] = weight((double)qr[x] - (double)pr[x]);
+        tok = draw(w, n, (double)u_res);
     }
     if (tok < 0) {
-        for (int x = 0; x < n; ++x) W[x] = fixed40(qr[x]);
-        tok = draw_fixed(W, n, u_res);
+        for (int x = 0; x < n; ++x) w[x] = weight((double)qr[x]);
+        tok = draw(w, n, (double)u_res);
     }
-    free(W);
+    free(w);
     tokens[acc] = tok;
     for (int i = acc + 1; i <= k; ++i) tokens[i] = -1;
     return acc;

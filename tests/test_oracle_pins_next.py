@@ -78,9 +78,9 @@ def test_summaries_after_append_match_the_whole_cache(oracle_mod):
 
 # ---------------------------------------------------------------- f2 speculative sampling
 
-def _golden_spec():
+def _golden_spec(fname="spec_accept_cases.txt"):
     out = []
-    for line in open(os.path.join(HERE, "golden", "spec_accept_cases.txt")):
+    for line in open(os.path.join(HERE, "golden", fname)):
         line = line.strip()
         if not line or line.startswith("#"):
             continue
@@ -124,6 +124,28 @@ def test_spec_accept_output_follows_the_target_distribution(oracle_mod):
     alpha = np.minimum(p0, q0).sum()
     got = np.mean(nacc >= 1)
     assert abs(got - alpha) <= 5 * np.sqrt(alpha * (1 - alpha) / N)
+
+
+def test_spec_accept_rejection_draws_from_the_residual(oracle_mod):
+    """At a rejection the emitted token follows max(0, q - p) normalised (drafts are
+    forced to be rejected with u = 1 - 2^-24 on a draft whose p exceeds q), so tokens
+    with q <= p are never emitted and the others with frequencies within 5 sigma."""
+    rng = np.random.default_rng(42)
+    n, N = 8, 40000
+    p = rng.dirichlet(np.ones(n)).astype(np.float32)
+    q = rng.dirichlet(np.ones(n)).astype(np.float32)
+    x = int(np.argmax(p.astype(np.float64) - q))       # a draft the target likes less
+    P = np.broadcast_to(p, (N, 1, n))
+    Q = np.broadcast_to(np.stack([q, q]), (N, 2, n))
+    u_acc = np.full((N, 1), np.float32(1 - 2.0 ** -24))  # u * p(x) >= q(x): rejected
+    nacc, toks = oracle_mod.spec_accept(P, Q, np.full((N, 1), x), u_acc, rng.random(N, dtype=np.float32))
+    assert np.all(nacc == 0)
+    r = np.maximum(0.0, q.astype(np.float64) - p)
+    r /= r.sum()
+    freq = np.bincount(toks[:, 0], minlength=n) / N
+    assert np.all(freq[r == 0] == 0)
+    sigma = np.sqrt(r * (1 - r) / N)
+    assert np.all(np.abs(freq - r) <= 5 * sigma + 1e-9), (freq, r)
 
 
 def test_spec_accept_identical_distributions_accept_everything(oracle_mod):
