@@ -141,6 +141,19 @@ const char *spd_last_error(void);
  */
 spd_status spd_device_status(uint32_t *out, int32_t clear);
 
+/*
+ * Limit, in nanoseconds of the GPU's global timer, of every bounded wait in the
+ * kernels launched after this call, from any host thread (2 s by default): an
+ * mbarrier wait on an asynchronous copy, and in sparse_decode_step's chain a
+ * selection waiting for its row's scores or an attention unit waiting for its
+ * row's selection.  A wait that runs out sets SPD_DEV_TIMEOUT, the kernel
+ * skips the rest of the affected rows and returns; the workspace of such a
+ * call must be zeroed again before it is reused.  Graphs keep the limit they
+ * were captured with.  ns = 0 is rejected (SPD_ERR_INVALID_ARG).
+ */
+spd_status spd_set_wait_limit_ns(uint64_t ns);
+uint64_t spd_wait_limit_ns(void);
+
 /* Workspace sizes in bytes (0 on invalid arguments; see spd_last_error). */
 size_t spd_score_select_workspace_size(const spd_dims *dims);
 size_t spd_sparse_decode_workspace_size(const spd_dims *dims, int32_t k_max, int32_t num_splits);

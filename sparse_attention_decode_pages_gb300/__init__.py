@@ -22,7 +22,7 @@ __all__ = [
     "sparse_decode_attn", "sparse_decode_attn_noalloc", "sparse_decode_step", "dense_verify_attn",
     "lse_merge", "spec_accept", "spd_device_status", "spd_score_select_workspace_size",
     "spd_sparse_decode_workspace_size", "spd_dense_verify_workspace_size",
-    "spd_sparse_decode_step_workspace_size",
+    "spd_sparse_decode_step_workspace_size", "spd_set_wait_limit_ns", "spd_wait_limit_ns",
     "DEV_BAD_PAGE", "DEV_BAD_SEL", "DEV_TIMEOUT", "DEV_BAD_LEN", "DEV_BAD_TOKEN",
 ]
 
@@ -93,6 +93,8 @@ def lib():
         L.spd_version.restype = i32
         L.spd_last_error.restype = ctypes.c_char_p
         L.spd_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+        L.spd_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        L.spd_wait_limit_ns.restype = ctypes.c_uint64
         L.spd_score_select_workspace_size.argtypes = [DP]
         L.spd_score_select_workspace_size.restype = sz
         L.spd_sparse_decode_workspace_size.argtypes = [DP, i32, i32]
@@ -118,7 +120,7 @@ def lib():
         L.spd_round_launch.argtypes = [P, i32, P]
         L.spd_round_destroy.argtypes = [P]
         L.spd_round_destroy.restype = None
-        for f in ("spd_device_status", "pages_summarize", "pages_score_select",
+        for f in ("spd_device_status", "spd_set_wait_limit_ns", "pages_summarize", "pages_score_select",
                   "sparse_decode_attn", "dense_verify_attn", "lse_merge",
                   "sparse_decode_attn_noalloc", "kv_append_refresh", "spec_accept",
                   "pages_append_score_select", "sparse_decode_step",
@@ -195,6 +197,16 @@ def spd_device_status(clear: bool = False) -> int:
     v = ctypes.c_uint32(0)
     _check(lib().spd_device_status(ctypes.byref(v), 1 if clear else 0))
     return v.value
+
+
+def spd_set_wait_limit_ns(ns: int):
+    """Limit (ns) of every bounded wait in kernels launched from now on (2 s by default)."""
+    _check(lib().spd_set_wait_limit_ns(int(ns)))
+
+
+def spd_wait_limit_ns() -> int:
+    """The current limit of the kernels' bounded waits, in nanoseconds."""
+    return int(lib().spd_wait_limit_ns())
 
 
 def pages_summarize(dims: Dims, K, page_table, seq_lens, summ, only_pages=None, stream=None):

@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
         auto slot_free = [&](long long jj) -> bool {
             bool r = true;
             if (lane == 0 && jj >= STAGES)
-                r = mbar_wait_bounded(empty + (jj % STAGES), (uint32_t)(((jj / STAGES) - 1) & 1), a.status);
+                r = mbar_wait_bounded(empty + (jj % STAGES), (uint32_t)(((jj / STAGES) - 1) & 1), a.status, a.wait_ns);
             return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
         };
         bool first_unit = true;
@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
                 // acquires it (so its own loads below are ordered after the
                 // selection's writes) and the TMA issuer fences the async proxy
                 bool okw = true;
-                if (lane == 0) okw = flag_wait_bounded(a.sel_done + row, 1u, a.status);
+                if (lane == 0) okw = flag_wait_bounded(a.sel_done + row, 1u, a.status, a.wait_ns);
                 if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) {
                     ok = false;
                     break;
@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
             if (seq >= C::NQ) {  // the unit-info entry and Q buffer of unit seq - NQ must be free
                 bool r = true;
                 if (lane == 0)
-                    r = mbar_wait_bounded(qempty + seq % C::NQ, (uint32_t)(((seq / C::NQ) - 1) & 1), a.status);
+                    r = mbar_wait_bounded(qempty + seq % C::NQ, (uint32_t)(((seq / C::NQ) - 1) & 1), a.status, a.wait_ns);
                 if (!__shfl_sync(0xffffffffu, r ? 1 : 0, 0)) {
                     ok = false;
                     break;
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
 
     for (long long j = kg;; j += KS) {
         const int slot = (int)(j % STAGES);
-        if (!mbar_wait_bounded(full + slot, (uint32_t)((j / STAGES) & 1), a.status)) break;
+        if (!mbar_wait_bounded(full + slot, (uint32_t)((j / STAGES) & 1), a.status, a.wait_ns)) break;
         const int2 meta = slot_meta[slot];
         if (meta.x == kEndOfWork) break;
         if (meta.y != cur_seq) {
@@ -533,7 +533,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
             ++units_done;
             if (kg > 0) {
                 // the previous unit's state must have been read before it is overwritten
-                if (units_done > 1 && !mbar_wait_bounded(merge_empty, ph ^ 1u, a.status)) break;
+                if (units_done > 1 && !mbar_wait_bounded(merge_empty, ph ^ 1u, a.status, a.wait_ns)) break;
                 float* dst = mb + ((long long)((kg - 1) * NMT + mt) * 32 + lane) * C::MERGE_FLOATS;
 #pragma unroll
                 for (int i = 0; i < NT_O; ++i)
@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
                 if (lane == 0) mbar_arrive(merge_full);
                 continue;
             }
-            if (!mbar_wait_bounded(merge_full, ph, a.status)) break;
+            if (!mbar_wait_bounded(merge_full, ph, a.status, a.wait_ns)) break;
 #pragma unroll 1
             for (int g = 1; g < KS; ++g) {
                 const float* src = mb + ((long long)((g - 1) * NMT + mt) * 32 + lane) * C::MERGE_FLOATS;

@@ -17,9 +17,9 @@ typedef __nv_bfloat16 bf16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// A wait on an asynchronous copy gives up after this long (nanoseconds of the
-// global timer), records SPD_DEV_TIMEOUT and lets the kernel return.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// Every wait gives up after `limit` nanoseconds of the global timer (a launch
+// argument: spd_set_wait_limit_ns, 2 s by default), records SPD_DEV_TIMEOUT and
+// lets the kernel return.
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -41,7 +41,8 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 
 // Waits (bounded, like the mbarrier waits) until *flag >= value, with acquire
 // semantics at GPU scope; false (and SPD_DEV_TIMEOUT) if it never happens.
-__device__ __forceinline__ bool flag_wait_bounded(const unsigned* flag, unsigned value, unsigned* status);
+__device__ __forceinline__ bool flag_wait_bounded(const unsigned* flag, unsigned value, unsigned* status,
+                                                  unsigned long long limit);
 
 __device__ __forceinline__ void raise_status(unsigned* status, unsigned bits) {
     if (status) atomicOr(status, bits);
@@ -88,13 +89,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false (and
-// sets SPD_DEV_TIMEOUT) if it has not completed within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned* status) {
+// sets SPD_DEV_TIMEOUT) if it has not completed within `limit` ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned* status,
+                                                  unsigned long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit) {
             raise_status(status, SPD_DEV_TIMEOUT);
             return false;
         }
@@ -135,26 +137,28 @@ __device__ __forceinline__ void red_relaxed_add(unsigned* p, unsigned v) {
 
 // As flag_wait_bounded, with relaxed loads (no ordering: for a progress count
 // whose data is checked on its own).
-__device__ __forceinline__ bool count_wait_bounded(const unsigned* cnt, unsigned value, unsigned* status) {
+__device__ __forceinline__ bool count_wait_bounded(const unsigned* cnt, unsigned value, unsigned* status,
+                                                   unsigned long long limit) {
     if (ld_relaxed(cnt) >= value) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
         __nanosleep(64);
         if (ld_relaxed(cnt) >= value) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit) {
             raise_status(status, SPD_DEV_TIMEOUT);
             return false;
         }
     }
 }
 
-__device__ __forceinline__ bool flag_wait_bounded(const unsigned* flag, unsigned value, unsigned* status) {
+__device__ __forceinline__ bool flag_wait_bounded(const unsigned* flag, unsigned value, unsigned* status,
+                                                  unsigned long long limit) {
     if (ld_acquire(flag) >= value) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
         __nanosleep(128);
         if (ld_acquire(flag) >= value) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit) {
             raise_status(status, SPD_DEV_TIMEOUT);
             return false;
         }

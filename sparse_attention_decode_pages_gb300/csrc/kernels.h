@@ -58,6 +58,11 @@ struct AppendArgs {
 };
 cudaError_t launch_append_refresh(const AppendArgs& a, cudaStream_t st);
 
+// Default limit of every bounded wait in the kernels (spd_set_wait_limit_ns).
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+// The limit the next launches pass to their kernels.
+unsigned long long wait_limit_ns();
+
 struct SpecArgs {
     const float* p;        // [B][k][n] drafter probabilities
     const float* q;        // [B][k+1][n] target probabilities
@@ -69,6 +74,7 @@ struct SpecArgs {
     int B, k;
     long long n;
     unsigned* status;
+    unsigned long long wait_ns;
 };
 cudaError_t launch_spec_accept(const SpecArgs& a, cudaStream_t st);
 size_t spec_smem_bytes(long long n);
@@ -103,6 +109,7 @@ struct ScoreSelectArgs {
     // [B*H_kv][max_pages] order-preserving score keys (never 0), zero on entry and
     // on exit: a key is its own ready flag, so the scoring warps need no fences
     unsigned* keys;
+    unsigned long long wait_ns;  // limit of every bounded wait
 };
 // Scores every page (persistent grid sized to num_sms), then selects per row.
 cudaError_t launch_score_select(const ScoreSelectArgs& a, int num_sms, cudaStream_t st);
@@ -127,6 +134,7 @@ struct AttnArgs {
     int num_sms;
     unsigned* status;
     unsigned* sel_done;  // chained step: wait for the row's selection flag instead of the previous grid
+    unsigned long long wait_ns;  // limit of every bounded wait
 };
 // Rows (T * G) handled per CTA, padded to 16-row MMA tiles.
 inline int attn_mtiles(int T, int G) {

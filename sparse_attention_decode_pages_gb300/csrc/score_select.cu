@@ -299,7 +299,7 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
         // The count is a hint (an unordered add); each key is its own ready flag, so
         // the keys are gathered into shared memory and any still 0 is read again.
         const int P0 = max(0, seq_pages(a.seq_lens[b], a.ps, a.max_pages));  // as the scoring kernel counts
-        if (tid == 0) s_ok = count_wait_bounded(a.tiles_done + row, (unsigned)((P0 + 15) / 16), a.status);
+        if (tid == 0) s_ok = count_wait_bounded(a.tiles_done + row, (unsigned)((P0 + 15) / 16), a.status, a.wait_ns);
         __syncthreads();
         if (!s_ok) return;
         unsigned* kg = a.keys + (long long)row * a.max_pages;
@@ -308,7 +308,7 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
         while (true) {
             if (!__syncthreads_or(missing)) break;
             if (tid == 0) {
-                s_ok = globaltimer_ns() - t0 <= kWaitLimitNs;
+                s_ok = globaltimer_ns() - t0 <= a.wait_ns;
                 if (!s_ok) raise_status(a.status, SPD_DEV_TIMEOUT);
             }
             __syncthreads();
@@ -835,11 +835,11 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
         int b, h, p0, P;
         locate(g, b, h, p0, P);
         const int row = b * a.H_kv + h;
-        if (!mbar_wait_bounded(bars + slot, (uint32_t)((t / kScoreStages) & 1), a.status)) {
+        if (!mbar_wait_bounded(bars + slot, (uint32_t)((t / kScoreStages) & 1), a.status, a.wait_ns)) {
             // Let the copies still in flight land (bounded) before giving up.
             for (int k2 = t + 1; k2 < t + kScoreStages; ++k2)
                 if (gq[k2 % kScoreStages] >= 0)
-                    mbar_wait_bounded(bars + (k2 % kScoreStages), (uint32_t)((k2 / kScoreStages) & 1), a.status);
+                    mbar_wait_bounded(bars + (k2 % kScoreStages), (uint32_t)((k2 / kScoreStages) & 1), a.status, a.wait_ns);
             break;
         }
         const uint8_t* sl = ring + slot * SLOT;

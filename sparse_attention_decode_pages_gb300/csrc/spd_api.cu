@@ -2,6 +2,7 @@
 // validation, workspace carving, TMA tensor-map encoding, launch-shape choice
 // and dispatch to the kernels.  Nothing here allocates device memory or
 // synchronises (except spd_device_status).
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -108,6 +109,12 @@ spd_status kv_map(CUtensorMap* m, const void* base, const spd_dims* d) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+namespace {
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+}  // namespace
+
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 
 // Per-device set-up of the current device (status word, SM count), done once.
 spd_status device_ready() {
@@ -225,6 +232,14 @@ using namespace spd;
 SPD_API int32_t spd_version(void) { return 100; }
 
 SPD_API const char* spd_last_error(void) { return g_err.c_str(); }
+
+SPD_API spd_status spd_set_wait_limit_ns(uint64_t ns) {
+    if (ns == 0) return fail(SPD_ERR_INVALID_ARG, "wait limit 0");
+    g_wait_ns.store(ns, std::memory_order_relaxed);
+    return SPD_OK;
+}
+
+SPD_API uint64_t spd_wait_limit_ns(void) { return wait_limit_ns(); }
 
 SPD_API spd_status spd_device_status(uint32_t* out, int32_t clear) {
     if (!out) return fail(SPD_ERR_INVALID_ARG, "out is NULL");
@@ -363,6 +378,7 @@ SPD_API spd_status spec_accept(int32_t B, int32_t k, int32_t n_vocab, const floa
     a.k = k;
     a.n = n_vocab;
     a.status = d->status;
+    a.wait_ns = wait_limit_ns();
     cudaError_t e = launch_spec_accept(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SPD_OK : cuda_fail(e, "spec_accept launch");
 }
@@ -416,6 +432,7 @@ static spd_status score_select_setup(const spd_dims* dims, const spd_bf16* q, co
     a.max_pages = dims->max_pages_per_seq;
     a.num_phys = dims->num_phys_pages;
     a.status = d->status;
+    a.wait_ns = wait_limit_ns();
     *dev = d;
     return SPD_OK;
 }
@@ -506,6 +523,7 @@ static spd_status sparse_attn_launch(const spd_dims* dims, const spd_bf16* q, co
     a.queue = w.queue;
     a.num_sms = d->sms;
     a.status = d->status;
+    a.wait_ns = wait_limit_ns();
     a.sel_done = sel_done;
     cudaError_t e = launch_sparse_attn(a, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SPD_OK : cuda_fail(e, "sparse attention launch");
@@ -654,6 +672,7 @@ SPD_API spd_status dense_verify_attn(const spd_dims* dims, int32_t T, const spd_
     a.queue = w.queue;
     a.num_sms = d->sms;
     a.status = d->status;
+    a.wait_ns = wait_limit_ns();
     cudaError_t e = launch_dense_attn(a, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SPD_OK : cuda_fail(e, "dense_verify_attn launch");
 }

@@ -186,7 +186,7 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
                 for (int c = 0; c < kSpecStages && c < nchunks; ++c) issue(c);
             for (int c = 0; c < nchunks; ++c) {
                 const int slot = (int)((chunks_done + c) % kSpecStages);
-                if (!dead && !mbar_wait_bounded(bars + slot, ((chunks_done + c) / kSpecStages) & 1u, a.status))
+                if (!dead && !mbar_wait_bounded(bars + slot, ((chunks_done + c) / kSpecStages) & 1u, a.status, a.wait_ns))
                     dead = true;
                 // warp w sums tiles w, w + NW, ... of the chunk
                 const long long s0 = e0 + (long long)c * kSpecChunk;

@@ -103,3 +103,15 @@ def test_product_path_does_not_reference_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "liboracle" not in text, f
+
+
+def test_wait_limit_setting(libspd):
+    """The limit of the kernels' bounded waits is a setting (no GPU needed to set it)."""
+    L = libspd.lib()
+    assert libspd.spd_wait_limit_ns() == 2_000_000_000
+    assert L.spd_set_wait_limit_ns(0) == 1 and b"wait limit" in L.spd_last_error()
+    try:
+        libspd.spd_set_wait_limit_ns(1_000_000)
+        assert libspd.spd_wait_limit_ns() == 1_000_000
+    finally:
+        libspd.spd_set_wait_limit_ns(2_000_000_000)

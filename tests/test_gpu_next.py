@@ -489,6 +489,61 @@ def test_decode_step_against_the_oracle(case):
         assert not nsel.cpu().numpy()[empty].any()
 
 
+def test_decode_step_wait_runs_out_and_the_next_call_is_clean():
+    """A bounded wait that runs out, on purpose and safely: a step workspace whose two
+    tile counters start past the end, so each scoring warp scores its fixed first
+    chunk and no more.  The rows beyond those chunks never get all their scores, so
+    their selections (waiting for the scores) and attention units (waiting for the
+    selections) give up after a 1 ms limit.  The call returns, SPD_DEV_TIMEOUT is set,
+    and the same step on a fresh zeroed workspace then gives the bits of a clean run
+    on a fresh cache (the append writes the same token again)."""
+    import torch
+    import sparse_attention_decode_pages_gb300 as spd
+    w = wl.named("q8b", threads=8, len_lo=3000, len_hi=6000)
+    k_new, v_new = _new_tokens(w, 1, 41)
+    kn = torch.from_numpy(k_new).view(torch.bfloat16).cuda()
+    vn = torch.from_numpy(v_new).view(torch.bfloat16).cuda()
+
+    def setup():
+        g = Gpu(w)
+        summ = g.summarize()
+        out = dict(sel=torch.full((w.B, w.H_kv, w.k_max), -1, dtype=torch.int32, device="cuda"),
+                   nsel=torch.full((w.B, w.H_kv), -7, dtype=torch.int32, device="cuda"),
+                   o=torch.full((w.B, w.H_q, w.D), float("nan"), dtype=torch.bfloat16, device="cuda"),
+                   lse=torch.full((w.B, w.H_q), float("nan"), device="cuda"))
+        return g, summ, out
+
+    def step(g, summ, out, ws):
+        d = g.d
+        spd.sparse_decode_step(g.dims, d["K"], d["V"], d["page_table"], d["seq_lens"], kn, vn, d["q"], summ,
+                               w.policy, out["sel"], out["nsel"], w.k_max, out["o"], ws, lse=out["lse"])
+        torch.cuda.synchronize()
+
+    def bits(g, summ, out):
+        return [_bits(g.d["K"]), summ_bits(summ), out["sel"].cpu().numpy(), out["nsel"].cpu().numpy(),
+                _bits(out["o"]), out["lse"].view(torch.int32).cpu().numpy()]
+
+    g, summ, out = setup()
+    ws_bytes = spd.spd_sparse_decode_step_workspace_size(g.dims, w.k_max)
+    ws = g.ws(ws_bytes)
+    chain = -(-spd.spd_score_select_workspace_size(g.dims) // 256) * 256  # the chain part of the workspace
+    ws[chain:chain + 16].view(torch.int64).fill_(1 << 40)                 # both tile counters past the end
+    spd.spd_set_wait_limit_ns(1_000_000)
+    try:
+        step(g, summ, out, ws)
+    finally:
+        spd.spd_set_wait_limit_ns(2_000_000_000)
+    st = spd.spd_device_status(clear=True)
+    assert st & spd.DEV_TIMEOUT, st
+    step(g, summ, out, g.ws(ws_bytes))               # a fresh zeroed workspace
+    assert spd.spd_device_status(clear=True) == 0
+    g2, summ2, out2 = setup()
+    step(g2, summ2, out2, g2.ws(ws_bytes))            # a clean run
+    assert spd.spd_device_status(clear=True) == 0
+    for x, y, what in zip(bits(g, summ, out), bits(g2, summ2, out2), ["K", "summ", "sel", "nsel", "o", "lse"]):
+        assert np.array_equal(x, y), what
+
+
 def test_decode_step_ties_go_to_lower_pages():
     """Pages with identical keys score alike: the chained step takes the mandatory pages
     and then the lowest page ids, at 41 and at 100 pages per row."""
