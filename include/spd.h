@@ -170,7 +170,12 @@ size_t spd_dense_verify_workspace_size(const spd_dims *dims, int32_t T, int32_t 
  *   summ[b][h][p][0][d] = min_t K[phys][h][t][d],  summ[b][h][p][1][d] = max_t ...
  * summ is bf16 [B][H_kv][max_pages_per_seq][2][D], sequence-major so that
  * scoring a (sequence, KV head) row reads one contiguous stream; bf16 min/max
- * is exact.
+ * is exact.  Sequences that share physical pages (the rollouts of one prompt
+ * sharing its prefix pages) each keep their own copy of a shared page's
+ * summary: the scoring reads each sharer's copy once per step either way, but
+ * the copies cost memory (4 * D bytes per page and KV head per sharer) and a
+ * rewritten shared page must be summarised again for every sharer (one
+ * only_pages entry per (sequence, page) slot).
  * only_pages: NULL = every logical page of every sequence; otherwise n_only
  * entries, each b * max_pages_per_seq + p (a slot of page_table), e.g. the
  * page the newest token was written to.  Entries whose p is past the

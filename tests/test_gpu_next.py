@@ -577,3 +577,53 @@ def test_decode_step_ties_go_to_lower_pages():
             assert nsel_h[b, h] == 8
             assert sel_h[b, h].tolist() == expect, (b, h, sel_h[b, h].tolist())
             assert ref["sel"][b, h, :8].tolist() == expect
+
+
+def test_rollouts_sharing_prompt_pages():
+    """A group of rollouts of one prompt (as in a GRPO group) shares the prompt's
+    physical pages: every sequence's page table points at the same 21 prefix pages,
+    followed by pages of its own.  The summaries are stored per sequence, so each
+    sharer gets its own copy of a shared page's summary: the copies are identical
+    and equal the oracle's; the one-call decode step (each sequence appending to a
+    page of its own) then matches the oracle on every sequence."""
+    import torch
+    import sparse_attention_decode_pages_gb300 as spd
+    ps, H_q, H_kv, D, shared = 16, 8, 2, 128, 21
+    lens = [shared * ps + 3, shared * ps + 40, shared * ps + 200, shared * ps + 517]
+    pol = wl.BudgetPolicy("fixed", fixed_pages=12, sink_pages=1, local_pages=2)
+    w = custom(lens, H_q, H_kv, D, ps, rng=np.random.default_rng(71), policy=pol, k_max=12)
+    for b in range(1, w.B):        # sequences 1.. reuse sequence 0's prompt pages
+        w.page_table[b, :shared] = w.page_table[0, :shared]
+    k_new, v_new = _new_tokens(w, 1, 72)
+    K2, V2 = oracle.append(w, 1, k_new, v_new)   # appends land in pages of each sequence's own
+    import dataclasses
+    w2 = dataclasses.replace(w, K=K2, V=V2)
+    ref = oracle.decode_step(w2, threads=4)
+    g = Gpu(w)
+    summ = g.summarize()
+    d = g.d
+    got = summ_bits(summ)
+    for b in range(1, w.B):
+        assert np.array_equal(got[b, :, :shared], got[0, :, :shared]), b
+    kn = torch.from_numpy(k_new).view(torch.bfloat16).cuda()
+    vn = torch.from_numpy(v_new).view(torch.bfloat16).cuda()
+    sel = torch.full((w.B, w.H_kv, w.k_max), -1, dtype=torch.int32, device="cuda")
+    nsel = torch.full((w.B, w.H_kv), -7, dtype=torch.int32, device="cuda")
+    o = torch.full((w.B, w.H_q, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((w.B, w.H_q), float("nan"), device="cuda")
+    ws = g.ws(spd.spd_sparse_decode_step_workspace_size(g.dims, w.k_max))
+    spd.sparse_decode_step(g.dims, d["K"], d["V"], d["page_table"], d["seq_lens"], kn, vn, d["q"], summ,
+                           w.policy, sel, nsel, w.k_max, o, ws, lse=lse)
+    assert g.sync_status() == 0
+    got = summ_bits(summ)
+    for b in range(w.B):
+        for p in range(w.pages(b)):
+            exp = wl.f32_to_bf16_bits(ref["summ"][w.page_table[b, p]].astype(np.float32))
+            assert np.array_equal(got[b, :, p], exp), (b, p)
+    _, _, sc, _ = g.score_select(summ)
+    same = compare_selection(w2, sel.cpu().numpy(), nsel.cpu().numpy(), sc.cpu().numpy(), ref["sel"],
+                             ref["nsel"], ref["scores"])
+    rows = [b for b in range(w.B) if all((b, h) in same for h in range(w.H_kv))]
+    assert len(rows) >= 3
+    assert_close_outputs(np_bf16(o)[rows], ref["o"][rows], lse.cpu().numpy()[rows], ref["lse"][rows],
+                         what="shared prompt pages")
