@@ -28,8 +28,9 @@
 // under the swizzle), online softmax in fp32 with exp2.  A unit that is a
 // whole row writes o / lse directly; otherwise it writes a normalised partial
 // and the last unit of the row to finish (an atomic ticket; nothing waits)
-// merges the partials with the log-sum-exp rule.  The last producer to run out
-// of units resets the queue, so the workspace counters are zero again on exit.
+// merges the partials with the log-sum-exp rule.  The producer making the grid's
+// last unit claim resets the queue, so the workspace counters are zero again on
+// exit.
 // Every wait is bounded (SPD_DEV_TIMEOUT on expiry).
 #pragma once
 
@@ -141,7 +142,9 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
     if (warp == C::CONSUMERS) {
         // ============================================================ producer warp
         const long long total_units = (long long)a.B * a.H_kv * a.num_splits;
-        int* queue = a.queue;  // [0..1] 64-bit unit counter, [2] producers finished
+        // [0..1] 64-bit unit counter: every producer claims units after its first until
+        // a claim fails, so the counter takes exactly total_units claims in all
+        int* queue = a.queue;
         long long j = 0;       // items issued
         int seq = 0;           // units issued
         bool ok = true;
@@ -158,7 +161,13 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
             // later ones come from the queue, which counts past the grid.
             unsigned long long u = blockIdx.x;
             if (!first_unit) {
-                if (lane == 0) u = gridDim.x + atomicAdd(reinterpret_cast<unsigned long long*>(queue), 1ull);
+                if (lane == 0) {
+                    unsigned long long* ctr = reinterpret_cast<unsigned long long*>(queue);
+                    u = gridDim.x + atomicAdd(ctr, 1ull);
+                    // the grid's last claim: every other claim has been made, so the
+                    // counter can be reset for the next call here
+                    if ((long long)u == (long long)gridDim.x + total_units - 1) *ctr = 0ull;
+                }
                 u = __shfl_sync(0xffffffffu, u, 0);
             }
             first_unit = false;
@@ -328,16 +337,6 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
                 mbar_arrive_expect_tx(full + slot, 0);
             }
             ++j;
-        }
-        // The last producer to finish resets the queue for the next call.
-        if (lane == 0) {
-            __threadfence();
-            const unsigned prev = atomicAdd(reinterpret_cast<unsigned*>(queue + 2), 1u);
-            if (prev == gridDim.x - 1) {
-                *reinterpret_cast<unsigned long long*>(queue) = 0ull;
-                queue[2] = 0;
-                __threadfence();
-            }
         }
         return;
     }

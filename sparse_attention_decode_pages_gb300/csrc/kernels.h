@@ -130,7 +130,7 @@ struct AttnArgs {
     float* part_o;    // [B*H_kv][num_splits][R][D]
     float* part_lse;  // [B*H_kv][num_splits][R]
     int* counters;    // [B*H_kv] split tickets, zero on entry and on exit
-    int* queue;       // 16 bytes (8-aligned): unit queue + finished workers, zero on entry and exit
+    int* queue;       // 16 bytes (8-aligned): the unit queue counter, zero on entry and exit
     int num_sms;
     unsigned* status;
     unsigned* sel_done;  // chained step: wait for the row's selection flag instead of the previous grid

@@ -33,9 +33,9 @@
 // agree), so it already spreads them; as soon as the digit being refined holds
 // at most as many keys as the CTA has threads (after one pass, typically)
 // those keys are ranked pairwise by (key desc, page asc) instead; otherwise the
-// passes end on the exact k'-th key.  Pages above the boundary plus the boundary pages that rank (or, at an
-// exact key, the lowest-id pages equal to it) are compacted in ascending order
-// into sel[] with ballots.
+// passes end on the exact k'-th key.  Pages above the boundary plus the
+// boundary pages that rank (or, at an exact key, the lowest-id pages equal to
+// it) are compacted in ascending order into sel[] with ballots.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -294,6 +294,10 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
     const unsigned lt_mask = (1u << lane) - 1u;
     const int b = row / a.H_kv;
     __shared__ int s_ok;
+    // the ranked path's chosen-page bits and candidate count start clear (ordered
+    // before their use by the barriers in between)
+    for (int w = tid; w < (a.max_pages + 31) / 32; w += NT) s_chosen[w] = 0u;
+    if (tid == 0) s_ncol = 0;
     if (a.keys) {
         // chained step: wait for this row's tiles only, not for the whole scoring grid.
         // The count is a hint (an unordered add); each key is its own ready flag, so
@@ -490,16 +494,20 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
     if (ranked) {
         // The candidates whose key matches the refined prefix, ranked by (key desc,
         // page asc); the first `rem` of them are chosen.
-        for (int w = tid; w < (P + 31) / 32; w += NT) s_chosen[w] = 0u;
-        if (tid == 0) s_ncol = 0;
-        __syncthreads();
-        for (int p = tid; p < P; p += NT) {
-            if (mand(p)) continue;
-            const uint32_t u = keys[p];
-            if ((u & pmask) != prefix) continue;
-            const int at = atomicAdd(&s_ncol, 1);
-            col_key[at] = u;  // at < s_cnt <= NT
-            col_p[at] = p;
+        // (s_chosen and s_ncol were cleared at the start of the row)
+        for (int p0 = 0; p0 < P; p0 += NT) {
+            const int p = p0 + tid;
+            uint32_t u = 0;
+            const bool in = p < P && !mand(p) && ((u = keys[p]) & pmask) == prefix;
+            const unsigned bm = __ballot_sync(0xffffffffu, in);
+            int base = 0;
+            if (bm && lane == 0) base = atomicAdd(&s_ncol, __popc(bm));  // one atomic per warp
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (in) {
+                const int at = base + __popc(bm & lt_mask);  // < s_cnt <= NT
+                col_key[at] = u;
+                col_p[at] = p;
+            }
         }
         __syncthreads();
         const int m = s_ncol;
