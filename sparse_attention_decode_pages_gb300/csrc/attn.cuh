@@ -66,8 +66,14 @@ struct AttnCfg {
     // reuses one only after every consumer warp has read it (the qempty barriers).
     static constexpr int NQ = 2;
     static constexpr int FIFO = NQ;
+    // Sparse decode (one query position, the G <= 8 heads of a KV head in one
+    // tile) computes the transposed products S^T = K Q^T and O^T += V^T P^T, so
+    // the 16 tokens of a chunk fill the MMA rows and the heads its 8 columns:
+    // half the MMAs of the head-row form, whose 16 rows would hold G heads.
+    static constexpr bool TRS = SPARSE && NMT == 1;
+    static constexpr int OT = TRS ? D / 16 : D / 8;  // O accumulator tiles per lane
     // Per consumer lane of groups 1..KS-1: its O fragments, then m0, m1, l0, l1.
-    static constexpr int MERGE_FLOATS = 4 * (D / 8) + 4;
+    static constexpr int MERGE_FLOATS = 4 * OT + 4;
     static constexpr int MERGE = KS > 1 ? (KS - 1) * NMT * 32 * MERGE_FLOATS * 4 : 0;
     static constexpr int OFF_Q = STAGES * SLOT;
     static constexpr int OFF_MERGE = OFF_Q + NQ * KS * QBYTES;
@@ -90,11 +96,12 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
     using C = AttnCfg<D, PS, NMT, SPARSE, KS>;
     constexpr int STAGES = C::STAGES;
     constexpr int KSTEPS = D / 16;
-    constexpr int NT_O = D / 8;
+    constexpr int NT_O = C::OT;
     constexpr int HALVES = D / 64;
     constexpr int HALF_BYTES = PS * 128;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_flag;
+    __shared__ int2 s_items[32];  // producer: the current batch's {logical page, physical page}
 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem;
@@ -273,34 +280,36 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
                         }
                     }
                 }
-                // the next batch: its logical pages now, its page-table entries after a
-                // few of this batch's pages are issued (by then the pages have arrived)
+                // the next batch: its logical pages now; its page-table entries while this
+                // batch is issued (lane 0 reads its own after a few of its pages)
                 const int nbase = base + 32;
                 int lp_next = -1;
                 long long ph_next = -1;
-                bool ph_read = false;
                 if (nbase + lane < count)
                     lp_next = SPARSE ? a.sel[(long long)row * a.k_max + start + nbase + lane] : start + nbase + lane;
                 auto read_next_page_table = [&]() {
                     if (nbase + lane < count && lp_next >= 0 && lp_next < P)
                         ph_next = a.page_table[(long long)b * a.max_pages + lp_next];
-                    ph_read = true;
                 };
+                // Lane 0 issues the batch from shared memory (no shuffles per item); the
+                // other lanes read their next page-table entries meanwhile.
+                s_items[lane] = make_int2(lp, (int)phys);
+                __syncwarp();
                 const int nb = min(32, cpad - base);
-                for (int k = 0; k < nb; ++k) {
-                    if (k == 4 && nbase < count) read_next_page_table();
-                    const int lpk = __shfl_sync(0xffffffffu, lp, k);
-                    const long long pk = __shfl_sync(0xffffffffu, phys, k);
-                    if (!slot_free(j)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) {
+                if (lane == 0) {
+                    for (int k = 0; k < nb; ++k) {
+                        if (k == min(4, nb - 1)) read_next_page_table();
+                        const int2 it = s_items[k];
                         const int slot = (int)(j % STAGES);
-                        slot_meta[slot] = make_int2(lpk, seq);
+                        if (j >= STAGES &&
+                            !mbar_wait_bounded(empty + slot, (uint32_t)(((j / STAGES) - 1) & 1), a.status, a.wait_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        slot_meta[slot] = make_int2(it.x, seq);
                         // each group's first item of the unit carries that group's copy of Q
                         const bool first = (base + k < KS);
-                        uint32_t bytes = lpk >= 0 ? (uint32_t)C::SLOT : 0u;
+                        uint32_t bytes = it.x >= 0 ? (uint32_t)C::SLOT : 0u;
                         if (first) bytes += (uint32_t)(R * D * 2);
                         mbar_arrive_expect_tx(full + slot, bytes);
                         if (first) {  // the unit's Q rows: T runs of G*D contiguous bf16
@@ -310,19 +319,20 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
                                 bulk_load(qd + t * G * D * 2, qs + (((long long)b * a.T + t) * a.H_q + h * G) * D,
                                           (uint32_t)(G * D * 2), full + slot);
                         }
-                        if (lpk >= 0) {
+                        if (it.x >= 0) {  // the page's K and V tiles: one 3-D box each
                             uint8_t* dst = ring + slot * C::SLOT;
-                            const int y = (int)((pk * a.H_kv + h) * PS);
-#pragma unroll
-                            for (int hf = 0; hf < HALVES; ++hf) {
-                                tma_load_2d(dst + hf * HALF_BYTES, &tmK, hf * 64, y, full + slot);
-                                tma_load_2d(dst + C::TILE + hf * HALF_BYTES, &tmV, hf * 64, y, full + slot);
-                            }
+                            const int y = (it.y * a.H_kv + h) * PS;
+                            tma_load_3d(dst, &tmK, 0, y, 0, full + slot);
+                            tma_load_3d(dst + C::TILE, &tmV, 0, y, 0, full + slot);
                         }
+                        ++j;
                     }
-                    ++j;
+                } else {
+                    read_next_page_table();
                 }
-                if (!ph_read && nbase < count) read_next_page_table();
+                __syncwarp();
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                j = __shfl_sync(0xffffffffu, j, 0);
                 lp_raw = lp_next;
                 ph_raw = ph_next;
             }
@@ -377,13 +387,25 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
             c_item = 0;
             g_items = (cu.count + KS - 1) / KS;
             const uint8_t* qsm = qbuf + ((cur_seq % C::NQ) * KS + kg) * C::QBYTES;
+            if constexpr (C::TRS) {
+                // B fragments of Q^T (k = channel, n = head lane/4): k-step kk holds
+                // channels 16kk + 2(lane%4) + {0, 1} and the same + 8
+                const int hn = lane >> 2;
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-                const int d0 = kk * 16 + 2 * c4;
-                qa[kk][0] = qr0 < R ? *reinterpret_cast<const uint32_t*>(qsm + (qr0 * D + d0) * 2) : 0u;
-                qa[kk][1] = qr1 < R ? *reinterpret_cast<const uint32_t*>(qsm + (qr1 * D + d0) * 2) : 0u;
-                qa[kk][2] = qr0 < R ? *reinterpret_cast<const uint32_t*>(qsm + (qr0 * D + d0 + 8) * 2) : 0u;
-                qa[kk][3] = qr1 < R ? *reinterpret_cast<const uint32_t*>(qsm + (qr1 * D + d0 + 8) * 2) : 0u;
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const int d0 = kk * 16 + 2 * c4;
+                    qa[kk][0] = hn < R ? *reinterpret_cast<const uint32_t*>(qsm + (hn * D + d0) * 2) : 0u;
+                    qa[kk][1] = hn < R ? *reinterpret_cast<const uint32_t*>(qsm + (hn * D + d0 + 8) * 2) : 0u;
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const int d0 = kk * 16 + 2 * c4;
+                    qa[kk][0] = qr0 < R ? *reinterpret_cast<const uint32_t*>(qsm + (qr0 * D + d0) * 2) : 0u;
+                    qa[kk][1] = qr1 < R ? *reinterpret_cast<const uint32_t*>(qsm + (qr1 * D + d0) * 2) : 0u;
+                    qa[kk][2] = qr0 < R ? *reinterpret_cast<const uint32_t*>(qsm + (qr0 * D + d0 + 8) * 2) : 0u;
+                    qa[kk][3] = qr1 < R ? *reinterpret_cast<const uint32_t*>(qsm + (qr1 * D + d0 + 8) * 2) : 0u;
+                }
             }
             m0 = m1 = NEG_INF;
             l0 = l1 = 0.f;
@@ -414,6 +436,84 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
                 __syncwarp();
             }
             const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
+            if constexpr (C::TRS) {
+#pragma unroll
+                for (int cc = 0; cc < PS / 16; ++cc) {
+                    // S^T = K Q^T (rows: the chunk's 16 tokens; columns: heads), four
+                    // independent MMA chains over the k-steps
+                    float sc[4][4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+                    const int mi = lane >> 3, rr = lane & 7;
+                    {
+                        // A fragments of K: matrices (tokens 0-7 | 8-15) x (channels lo | hi)
+                        const int tok = cc * 16 + (mi & 1) * 8 + rr;
+#pragma unroll
+                        for (int kk = 0; kk < KSTEPS; ++kk) {
+                            const int chunk = 2 * kk + (mi >> 1);
+                            uint32_t ka[4];
+                            ldsm_x4(kbase + (chunk >> 3) * HALF_BYTES + swz128(tok, chunk & 7), ka[0], ka[1], ka[2], ka[3]);
+                            mma_bf16(sc[kk & 3], ka, qa[kk][0], qa[kk][1]);
+                        }
+                    }
+                    // lane: tokens g, g + 8 (g = lane/4) x heads 2c, 2c + 1 (c = lane%4)
+                    const int tok0 = page_start + cc * 16 + (lane >> 2);
+                    float x[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) x[e] = ((sc[0][e] + sc[1][e]) + (sc[2][e] + sc[3][e])) * a.scale_log2;
+                    if (tok0 > lim_min) x[0] = x[1] = NEG_INF;      // past the sequence end
+                    if (tok0 + 8 > lim_min) x[2] = x[3] = NEG_INF;
+                    // per-head maximum over the chunk's tokens (lanes with the same c)
+                    float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                    }
+                    // lazy rescaling, as in the head-row form (m0 / m1: heads 2c / 2c + 1)
+                    const bool up0 = mx0 > m0 + kRescale, up1 = mx1 > m1 + kRescale;
+                    if (__any_sync(0xffffffffu, up0 || up1)) {
+                        const float mn0 = up0 ? mx0 : m0, mn1 = up1 ? mx1 : m1;
+                        const float al0 = (m0 == NEG_INF) ? 0.f : fast_exp2(m0 - mn0);
+                        const float al1 = (m1 == NEG_INF) ? 0.f : fast_exp2(m1 - mn1);
+                        m0 = mn0;
+                        m1 = mn1;
+                        l0 *= al0;
+                        l1 *= al1;
+#pragma unroll
+                        for (int i = 0; i < NT_O; ++i) {
+                            oacc[i][0] *= al0;
+                            oacc[i][1] *= al1;
+                            oacc[i][2] *= al0;
+                            oacc[i][3] *= al1;
+                        }
+                    }
+                    const float base0 = m0 == NEG_INF ? 0.f : m0;
+                    const float base1 = m1 == NEG_INF ? 0.f : m1;
+                    x[0] = fast_exp2(x[0] - base0);
+                    x[1] = fast_exp2(x[1] - base1);
+                    x[2] = fast_exp2(x[2] - base0);
+                    x[3] = fast_exp2(x[3] - base1);
+                    l0 += x[0] + x[2];
+                    l1 += x[1] + x[3];
+                    // P^T as the B operand (k = token, n = head): each 8-token half of
+                    // the accumulator is one 8x8 fragment, transposed in registers
+                    const uint32_t pb0 = movmatrix_t(pack_bf16(x[0], x[1]));
+                    const uint32_t pb1 = movmatrix_t(pack_bf16(x[2], x[3]));
+                    {
+                        // A fragments of V^T: transposed loads of V's (tokens 0-7 | 8-15)
+                        // x (channels lo | hi) matrices
+                        const int tok = cc * 16 + (mi >> 1) * 8 + rr;
+#pragma unroll
+                        for (int np = 0; np < D / 16; ++np) {
+                            const int chunk = 2 * np + (mi & 1);
+                            uint32_t va[4];
+                            ldsm_x4_t(vbase + (chunk >> 3) * HALF_BYTES + swz128(tok, chunk & 7), va[0], va[1], va[2], va[3]);
+                            mma_bf16(oacc[np], va, pb0, pb1);
+                        }
+                    }
+                }
+            } else {
 #pragma unroll
             for (int cc = 0; cc < PS / 16; ++cc) {
                 // S = Q K^T: even and odd k-steps accumulate in separate chains (four
@@ -516,6 +616,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
                     }
                 }
             }
+            }
         }
         // This warp is done with the slot.
         __syncwarp();
@@ -555,10 +656,17 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
 #pragma unroll
                 for (int i = 0; i < NT_O; ++i) {
                     const float4 v = *reinterpret_cast<const float4*>(src + 4 * i);
-                    oacc[i][0] = oacc[i][0] * a0 + v.x * b0;
-                    oacc[i][1] = oacc[i][1] * a0 + v.y * b0;
-                    oacc[i][2] = oacc[i][2] * a1 + v.z * b1;
-                    oacc[i][3] = oacc[i][3] * a1 + v.w * b1;
+                    if constexpr (C::TRS) {  // elements 0, 2: head 2c; 1, 3: head 2c + 1
+                        oacc[i][0] = oacc[i][0] * a0 + v.x * b0;
+                        oacc[i][1] = oacc[i][1] * a1 + v.y * b1;
+                        oacc[i][2] = oacc[i][2] * a0 + v.z * b0;
+                        oacc[i][3] = oacc[i][3] * a1 + v.w * b1;
+                    } else {  // elements 0, 1: row qr0; 2, 3: row qr1
+                        oacc[i][0] = oacc[i][0] * a0 + v.x * b0;
+                        oacc[i][1] = oacc[i][1] * a0 + v.y * b0;
+                        oacc[i][2] = oacc[i][2] * a1 + v.z * b1;
+                        oacc[i][3] = oacc[i][3] * a1 + v.w * b1;
+                    }
                 }
                 l0 = l0 * a0 + st.z * b0;
                 l1 = l1 * a1 + st.w * b1;
@@ -568,14 +676,62 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
             __syncwarp();
             if (lane == 0) mbar_arrive(merge_empty);
         }
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        if constexpr (C::TRS) {  // a head's row sum is spread over the lanes of one c
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+            }
+        } else {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        }
         const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
         const float lse0 = l0 > 0.f ? (m0 + __log2f(l0)) * kLn2 : NEG_INF;
         const float lse1 = l1 > 0.f ? (m1 + __log2f(l1)) * kLn2 : NEG_INF;
-        if (cu.nsplit == 1) {
+        if constexpr (C::TRS) {
+            // lane: heads h0 = 2c, h1 = 2c + 1; channels 16i + g and 16i + g + 8
+            const int h0 = 2 * c4, h1 = h0 + 1, g = lane >> 2;
+            if (cu.nsplit == 1) {
+                bf16* o0 = reinterpret_cast<bf16*>(a.o) + out_index(cu.row, h0 < R ? h0 : 0) * D + g;
+                bf16* o1 = reinterpret_cast<bf16*>(a.o) + out_index(cu.row, h1 < R ? h1 : 0) * D + g;
+#pragma unroll
+                for (int i = 0; i < NT_O; ++i) {
+                    if (h0 < R) {
+                        o0[16 * i] = __float2bfloat16_rn(oacc[i][0] * inv0);
+                        o0[16 * i + 8] = __float2bfloat16_rn(oacc[i][2] * inv0);
+                    }
+                    if (h1 < R) {
+                        o1[16 * i] = __float2bfloat16_rn(oacc[i][1] * inv1);
+                        o1[16 * i + 8] = __float2bfloat16_rn(oacc[i][3] * inv1);
+                    }
+                }
+                if (g == 0 && a.lse) {
+                    if (h0 < R) a.lse[out_index(cu.row, h0)] = lse0;
+                    if (h1 < R) a.lse[out_index(cu.row, h1)] = lse1;
+                }
+                continue;
+            }
+            const long long pb = ((long long)cu.row * a.num_splits + cu.split) * R;
+#pragma unroll
+            for (int i = 0; i < NT_O; ++i) {
+                if (h0 < R) {
+                    a.part_o[(pb + h0) * D + 16 * i + g] = oacc[i][0] * inv0;
+                    a.part_o[(pb + h0) * D + 16 * i + g + 8] = oacc[i][2] * inv0;
+                }
+                if (h1 < R) {
+                    a.part_o[(pb + h1) * D + 16 * i + g] = oacc[i][1] * inv1;
+                    a.part_o[(pb + h1) * D + 16 * i + g + 8] = oacc[i][3] * inv1;
+                }
+            }
+            if (g == 0) {
+                if (h0 < R) a.part_lse[pb + h0] = lse0;
+                if (h1 < R) a.part_lse[pb + h1] = lse1;
+            }
+        } else {
+          if (cu.nsplit == 1) {
 #pragma unroll
             for (int i = 0; i < NT_O; ++i) {
                 const int d = i * 8 + 2 * c4;
@@ -606,6 +762,7 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
         if (c4 == 0) {
             if (qr0 < R) a.part_lse[pbase + qr0] = lse0;
             if (qr1 < R) a.part_lse[pbase + qr1] = lse1;
+        }
         }
         // Ticket: the partial writes of every consumer lane are ordered before one
         // acq_rel atomic (barrier, then release at GPU scope); the last unit of

@@ -89,17 +89,19 @@ EncodeTiledFn encode_fn(spd_status* st) {
     return fn;
 }
 
-// 2-D view of a paged K or V cache: rows = num_phys * H_kv * ps, D bf16 each;
-// box = ps rows x 64 elements (128 bytes), 128-byte swizzle.
+// 3-D view of a paged K or V cache: x = 64 channels (128 bytes), y = rows
+// (num_phys * H_kv * ps of D bf16, stride 2D bytes), z = the D / 64 halves of a
+// row (stride 128 bytes).  One box = a page's ps rows of one KV head, laid out
+// in shared memory as [half][row][64] with the 128-byte swizzle.
 spd_status kv_map(CUtensorMap* m, const void* base, const spd_dims* d) {
     spd_status st = SPD_OK;
     EncodeTiledFn fn = encode_fn(&st);
     if (!fn) return st;
-    cuuint64_t gdim[2] = {(cuuint64_t)d->D, (cuuint64_t)d->num_phys_pages * d->H_kv * d->page_size};
-    cuuint64_t gstride[1] = {(cuuint64_t)d->D * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)d->page_size};
-    cuuint32_t estride[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estride,
+    cuuint64_t gdim[3] = {64, (cuuint64_t)d->num_phys_pages * d->H_kv * d->page_size, (cuuint64_t)d->D / 64};
+    cuuint64_t gstride[2] = {(cuuint64_t)d->D * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)d->page_size, (cuuint32_t)d->D / 64};
+    cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box, estride,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(SPD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
