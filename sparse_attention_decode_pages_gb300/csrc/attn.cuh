@@ -203,8 +203,13 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
             }
             // The first 32 selection entries are loaded together with the length
             // and the count (one round trip instead of two).
-            int pre = -1;
-            if (SPARSE && start + lane < a.k_max) pre = a.sel[(long long)row * a.k_max + start + lane];
+            // (chained step: with their physical pages, so no page-table round trip follows)
+            const bool phys_given = SPARSE && a.sel_phys != nullptr;
+            int pre = -1, pre_ph = -1;
+            if (SPARSE && start + lane < a.k_max) {
+                pre = a.sel[(long long)row * a.k_max + start + lane];
+                if (phys_given) pre_ph = a.sel_phys[(long long)row * a.k_max + start + lane];
+            }
             const int len = a.seq_lens[b];
             int P = seq_pages(len, PS, a.max_pages);
             if (P < 0) {  // a length the page table cannot hold: the row is empty
@@ -262,7 +267,8 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
             long long ph_raw = -1;   // and its page-table entry (read when lp_raw is in range)
             if (lane < count) {
                 lp_raw = SPARSE ? pre : start + lane;
-                if (lp_raw >= 0 && lp_raw < P) ph_raw = a.page_table[(long long)b * a.max_pages + lp_raw];
+                if (lp_raw >= 0 && lp_raw < P)
+                    ph_raw = phys_given ? pre_ph : a.page_table[(long long)b * a.max_pages + lp_raw];
             }
             for (int base = 0; base < cpad && ok; base += 32) {
                 int lp = -1;
@@ -283,13 +289,15 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
                 // the next batch: its logical pages now; its page-table entries while this
                 // batch is issued (lane 0 reads its own after a few of its pages)
                 const int nbase = base + 32;
-                int lp_next = -1;
+                int lp_next = -1, ph_given = -1;
                 long long ph_next = -1;
-                if (nbase + lane < count)
+                if (nbase + lane < count) {
                     lp_next = SPARSE ? a.sel[(long long)row * a.k_max + start + nbase + lane] : start + nbase + lane;
+                    if (phys_given) ph_given = a.sel_phys[(long long)row * a.k_max + start + nbase + lane];
+                }
                 auto read_next_page_table = [&]() {
                     if (nbase + lane < count && lp_next >= 0 && lp_next < P)
-                        ph_next = a.page_table[(long long)b * a.max_pages + lp_next];
+                        ph_next = phys_given ? ph_given : a.page_table[(long long)b * a.max_pages + lp_next];
                 };
                 // Lane 0 issues the batch from shared memory (no shuffles per item); the
                 // other lanes read their next page-table entries meanwhile.

@@ -109,6 +109,9 @@ struct ScoreSelectArgs {
     // [B*H_kv][max_pages] order-preserving score keys (never 0), zero on entry and
     // on exit: a key is its own ready flag, so the scoring warps need no fences
     unsigned* keys;
+    // chained step: [B*H_kv][k_max] the physical page of each selected page (read by
+    // the attention instead of the page table); NULL otherwise
+    int32_t* sel_phys;
     unsigned long long wait_ns;  // limit of every bounded wait
 };
 // Scores every page (persistent grid sized to num_sms), then selects per row.
@@ -134,6 +137,7 @@ struct AttnArgs {
     int num_sms;
     unsigned* status;
     unsigned* sel_done;  // chained step: wait for the row's selection flag instead of the previous grid
+    const int32_t* sel_phys;  // chained step: physical pages of sel (NULL: look them up in page_table)
     unsigned long long wait_ns;  // limit of every bounded wait
 };
 // Rows (T * G) handled per CTA, padded to 16-row MMA tiles.

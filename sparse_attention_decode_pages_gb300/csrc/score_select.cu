@@ -276,7 +276,7 @@ __device__ __forceinline__ bool repoll_keys(const unsigned* kg, uint32_t* ks, in
     return missing;
 }
 
-// Selection of one (sequence, KV head) row by a CTA of 8 warps.  keys: the
+// Selection of one (sequence, KV head) row by a CTA of NT / 32 warps.  keys: the
 // dynamic shared memory (the row's order-preserving score keys, then bit words).
 template <int NT>
 __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const int row, uint32_t* keys) {
@@ -287,22 +287,36 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
     __shared__ int w_eq[NWARP], w_take[NWARP];
     __shared__ uint32_t col_key[NT];
     __shared__ int col_p[NT];
-    // after the keys: boundary pages chosen by rank, and the final decision (bit per page)
+    // after the keys: boundary pages chosen by rank and the final decision (a bit
+    // per page each), (top-p) the page weights, (chained step) the row's page table
+    const int words = (a.max_pages + 31) / 32;
     uint32_t* s_chosen = keys + a.max_pages;
-    uint32_t* s_take = s_chosen + (a.max_pages + 31) / 32;
+    uint32_t* s_take = s_chosen + words;
+    int32_t* s_pt = reinterpret_cast<int32_t*>(s_take + words + (a.pol.mode == SPD_BUDGET_TOP_P ? a.max_pages : 0));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned lt_mask = (1u << lane) - 1u;
     const int b = row / a.H_kv;
+    const int len = a.seq_lens[b];
     __shared__ int s_ok;
-    // the ranked path's chosen-page bits and candidate count start clear (ordered
-    // before their use by the barriers in between)
-    for (int w = tid; w < (a.max_pages + 31) / 32; w += NT) s_chosen[w] = 0u;
-    if (tid == 0) s_ncol = 0;
+    // the candidate count, the key range and the first radix level's histogram
+    // start clear (ordered before their use by the barriers in between; the
+    // previous row's last use ended at the barrier between rows)
+    if (tid == 0) {
+        s_ncol = 0;
+        s_kmin = 0xffffffffu;
+        s_kmax = 0u;
+    }
+    for (int i = tid; i < 256; i += NT) hist[i] = 0;
+    for (int w = tid; w < words; w += NT) s_chosen[w] = 0u;
     if (a.keys) {
         // chained step: wait for this row's tiles only, not for the whole scoring grid.
         // The count is a hint (an unordered add); each key is its own ready flag, so
         // the keys are gathered into shared memory and any still 0 is read again.
-        const int P0 = max(0, seq_pages(a.seq_lens[b], a.ps, a.max_pages));  // as the scoring kernel counts
+        const int P0 = max(0, seq_pages(len, a.ps, a.max_pages));  // as the scoring kernel counts
+        // the row's page-table entries, copied while the keys are awaited (for the
+        // physical page of each selected page)
+        if (a.sel_phys)
+            for (int p = tid; p < P0; p += NT) cp_async4(s_pt + p, a.page_table + (long long)b * a.max_pages + p);
         if (tid == 0) s_ok = count_wait_bounded(a.tiles_done + row, (unsigned)((P0 + 15) / 16), a.status, a.wait_ns);
         __syncthreads();
         if (!s_ok) return;
@@ -334,7 +348,6 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
         __syncthreads();
         if (tid == 0) st_release(a.sel_done + row, 1u);
     };
-    const int len = a.seq_lens[b];
     const int P = max(0, seq_pages(len, a.ps, a.max_pages));  // a bad length: empty (flagged by the scoring)
     int32_t* out = a.sel + (long long)row * a.k_max;
     if (P <= 0) {
@@ -352,11 +365,7 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
 
     // keys: each thread's loads are independent and issued back to back; the
     // candidates' smallest and largest key on the way
-    if (tid == 0) {
-        s_kmin = 0xffffffffu;
-        s_kmax = 0u;
-    }
-    __syncthreads();
+    if (!a.keys) __syncthreads();  // (chained: the waits above ordered the clearing)
     uint32_t kmin = 0xffffffffu, kmax = 0u;
     if (a.keys) {  // chained step: the keys are already in shared memory
         for (int p = tid; p < P; p += NT) {
@@ -399,8 +408,7 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
 
     long long k;
     if (a.pol.mode == SPD_BUDGET_TOP_P)
-        k = nm + top_p_pages<NT>(a, keys, P, mand, hist, s_digit, s_rem, s_kmin, s_kmax,
-                             s_take + (a.max_pages + 31) / 32);
+        k = nm + top_p_pages<NT>(a, keys, P, mand, hist, s_digit, s_rem, s_kmin, s_kmax, s_take + words);
     else
         k = budget_pages(a.pol, len, a.ps);
     if (k > a.k_max) k = a.k_max;
@@ -429,12 +437,16 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
         pmask = h < 0 ? 0xffffffffu : (h >= 31 ? 0u : ~((2u << h) - 1u));
         prefix = s_kmin & pmask;
         int ncnt = ncand;
+        bool clean = a.pol.mode != SPD_BUDGET_TOP_P;  // the first level's histogram is clear
         while (h >= 0 && ncnt > NT) {
             const int wd = h + 1 < 8 ? h + 1 : 8;
             const int shift = h + 1 - wd;
             const uint32_t dmask = (1u << wd) - 1u;
-            for (int i = tid; i < 256; i += NT) hist[i] = 0;
-            __syncthreads();
+            if (!clean) {
+                for (int i = tid; i < 256; i += NT) hist[i] = 0;
+                __syncthreads();
+            }
+            clean = false;
             for (int p0 = 0; p0 < P; p0 += NT) {
                 const int p = p0 + tid;
                 bool in = false;
@@ -567,6 +579,7 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
             eqb += __popc(eb);
         }
     }
+    if (a.sel_phys) cp_async_wait_all();  // this thread's page-table copies (the barrier: everyone's)
     if (lane == 0) w_take[warp] = n_take;
     __syncthreads();
     int pos = 0, total = 0;
@@ -577,7 +590,10 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
     for (int p0 = lo; p0 < hi; p0 += 32) {
         const unsigned tb = s_take[p0 >> 5];
         const int at = pos + __popc(tb & lt_mask);
-        if (((tb >> lane) & 1u) && at < a.k_max) out[at] = p0 + lane;
+        if (((tb >> lane) & 1u) && at < a.k_max) {
+            out[at] = p0 + lane;
+            if (a.sel_phys) a.sel_phys[(long long)row * a.k_max + at] = s_pt[p0 + lane];
+        }
         pos += __popc(tb);
     }
     if (tid == 0) {
@@ -949,9 +965,11 @@ cudaError_t launch_score_select(const ScoreSelectArgs& a, int num_sms, cudaStrea
     cudaError_t e = a.D == 128 ? launch_score_t<128>(a, grid, st) : launch_score_t<64>(a, grid, st);
     if (e != cudaSuccess) return e;
     // selection: one CTA per row, the row's keys in shared memory
-    // keys, chosen and decision bit words, and (top-p) the page weights
+    // keys, chosen and decision bit words, (top-p) the page weights, (chained) the
+    // page-table row
     const size_t smem = ((size_t)a.max_pages + 2 * (((size_t)a.max_pages + 31) / 32) +
-                         (a.pol.mode == SPD_BUDGET_TOP_P ? (size_t)a.max_pages : 0)) * sizeof(uint32_t);
+                         (a.pol.mode == SPD_BUDGET_TOP_P ? (size_t)a.max_pages : 0) +
+                         (a.sel_phys ? (size_t)a.max_pages : 0)) * sizeof(uint32_t);
     long long sgrid = (long long)a.B * a.H_kv;
     if (a.tiles_done) {
         // chained step: two 128-thread CTAs per SM, resident beside the scoring CTAs

@@ -488,8 +488,8 @@ static spd_status attn_common(const spd_dims* dims, const spd_bf16* q, const spd
 static spd_status sparse_attn_launch(const spd_dims* dims, const spd_bf16* q, const spd_bf16* K, const spd_bf16* V,
                                      const int32_t* page_table, const int32_t* seq_lens, const int32_t* sel,
                                      const int32_t* nsel, int32_t k_max, int S, float softmax_scale, spd_bf16* o,
-                                     float* lse, void* ws, size_t ws_bytes, unsigned* sel_done, DevInfo* d,
-                                     void* stream) {
+                                     float* lse, void* ws, size_t ws_bytes, unsigned* sel_done,
+                                     const int32_t* sel_phys, DevInfo* d, void* stream) {
     spd_status st;
     const int G = dims->H_q / dims->H_kv;
     const long long rows = (long long)dims->B * dims->H_kv;
@@ -527,6 +527,7 @@ static spd_status sparse_attn_launch(const spd_dims* dims, const spd_bf16* q, co
     a.status = d->status;
     a.wait_ns = wait_limit_ns();
     a.sel_done = sel_done;
+    a.sel_phys = sel_phys;
     cudaError_t e = launch_sparse_attn(a, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SPD_OK : cuda_fail(e, "sparse attention launch");
 }
@@ -547,21 +548,31 @@ SPD_API spd_status sparse_decode_attn(const spd_dims* dims, const spd_bf16* q, c
     if (!d) return st;
     return sparse_attn_launch(dims, q, K, V, page_table, seq_lens, sel, nsel, k_max,
                               sparse_splits(dims, k_max, num_splits, d->sms), softmax_scale, o, lse, ws, ws_bytes,
-                              nullptr, d, stream);
+                              nullptr, nullptr, d, stream);
 }
 
 // The chained step's workspace: [score / select][chain: two tile counters, warps
-// done, tiles_done[rows], sel_done[rows], (256-aligned) keys[rows][max_pages]][attention].
+// done, tiles_done[rows], sel_done[rows], (256-aligned) keys[rows][max_pages],
+// (256-aligned) sel_phys[rows][k_max]][attention].
 struct StepWs {
-    size_t score, chain, keys, attn, bytes;
+    size_t score, chain, keys, phys, attn, bytes;
 };
+
+// The chained selection also writes each selected page's physical page (from a copy
+// of the row's page table in shared memory) when that copy fits comfortably.
+static bool step_sel_phys(const spd_dims* dims, const spd_budget_policy* policy) {
+    const size_t words = ((size_t)dims->max_pages_per_seq + 31) / 32;
+    const size_t per = (policy && policy->mode == SPD_BUDGET_TOP_P) ? 3 : 2;
+    return ((size_t)dims->max_pages_per_seq * per + 2 * words) * sizeof(uint32_t) <= 96 * 1024;
+}
 
 static bool step_ws_layout(const spd_dims* dims, int32_t k_max, StepWs* w, DevInfo* d) {
     const long long rows = (long long)dims->B * dims->H_kv;
     const int S = sparse_splits(dims, k_max, 0, d->sms);
     w->score = align256(spd_score_select_workspace_size(dims));
     w->keys = align256(32 + 2 * (size_t)rows * sizeof(unsigned));  // offset of the keys in the chain part
-    w->chain = w->keys + align256((size_t)rows * dims->max_pages_per_seq * sizeof(unsigned));
+    w->phys = w->keys + align256((size_t)rows * dims->max_pages_per_seq * sizeof(unsigned));
+    w->chain = w->phys + align256((size_t)rows * k_max * sizeof(int32_t));
     w->attn = attn_ws_layout(nullptr, rows, S, dims->H_q / dims->H_kv, dims->D).bytes;
     w->bytes = w->score + w->chain + w->attn;
     return w->score != 0;
@@ -621,11 +632,15 @@ SPD_API spd_status sparse_decode_step(const spd_dims* dims, spd_bf16* K, spd_bf1
     a.tiles_done = reinterpret_cast<unsigned*>(chain + 32);
     a.sel_done = a.tiles_done + rows;
     a.keys = reinterpret_cast<unsigned*>(chain + w.keys);
+    if (step_sel_phys(dims, policy)) {
+        a.page_table = page_table;
+        a.sel_phys = reinterpret_cast<int32_t*>(chain + w.phys);
+    }
     unsigned* sel_done = a.sel_done;
     cudaError_t e = launch_score_select(a, d->sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sparse_decode_step scoring launch");
     return sparse_attn_launch(dims, q, K, V, page_table, seq_lens, sel, nsel, k_max, S, softmax_scale, o, lse,
-                              base + w.score + w.chain, w.attn, sel_done, d, stream);
+                              base + w.score + w.chain, w.attn, sel_done, a.sel_phys, d, stream);
 }
 
 SPD_API spd_status dense_verify_attn(const spd_dims* dims, int32_t T, const spd_bf16* q, const spd_bf16* K,
@@ -765,5 +780,5 @@ SPD_API spd_status sparse_decode_attn_noalloc(const spd_dims* dims, const spd_bf
     cudaError_t e = cudaMemsetAsync(scratch, 0, zero_bytes, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "clearing the fixed scratch array");
     return sparse_attn_launch(dims, q, K, V, page_table, seq_lens, sel, nsel, k_max, S, softmax_scale, o, lse,
-                              scratch, SPD_NOALLOC_SCRATCH_BYTES, nullptr, d, stream);
+                              scratch, SPD_NOALLOC_SCRATCH_BYTES, nullptr, nullptr, d, stream);
 }
