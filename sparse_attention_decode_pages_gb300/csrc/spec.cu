@@ -19,12 +19,14 @@
 //
 // The draw streams the row once.  Each CTA sums the 128-element tiles of its
 // share of the row into its shared memory: rows whose length is a multiple of
-// 4 arrive through a 2-deep ring of 16-tile chunks filled by bulk copies (each
+// 4 arrive through a 3-deep ring of 16-tile chunks filled by bulk copies (each
 // warp sums two tiles of each chunk); other rows through plain loads, a warp
-// per tile.  Eight 8-warp CTAs per sequence fit in one wave at B = 64.  After a cluster barrier, CTA 0 gathers every tile sum
-// through distributed shared memory and block-scans contiguous runs of them;
-// the one thread whose run holds the target finds the crossing tile, and a
-// warp scans that tile's 128 weights to find the element.
+// per tile.  Eight 8-warp CTAs per sequence fit in one wave at B = 64.  After a
+// cluster barrier every CTA reads the eight shares' sums through distributed
+// shared memory; the one CTA whose share holds the target block-scans its own
+// tile sums, the one thread whose run of tiles holds it finds the crossing
+// tile, a warp scans that tile's 128 weights to find the element, and the
+// token goes to CTA 0, which writes the outputs.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -41,7 +43,7 @@ constexpr int kSpecUnroll = 2;
 // n % 4 == 0 rows stream through shared memory: chunks of 16 tiles (q and p),
 // kSpecStages in flight per CTA, copied by the bulk-copy engine.
 constexpr int kSpecChunk = 16 * kSpecTile;  // elements
-constexpr int kSpecStages = 2;
+constexpr int kSpecStages = 3;
 constexpr size_t kSpecRingBytes = (size_t)kSpecStages * 2 * kSpecChunk * sizeof(float);
 typedef unsigned long long u64;
 
@@ -97,7 +99,7 @@ __device__ __forceinline__ u64 shfl_xor_u64(u64 v, int off) {
 template <bool VEC>
 __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThreads, 4)
     spec_accept_kernel(SpecArgs a) {
-    // [VEC: ring of kSpecStages x {q, p} chunks][tpc own tile sums][(CTA 0) ntiles all tile sums][VEC: bars]
+    // [VEC: ring of kSpecStages x {q, p} chunks][tpc own tile sums][VEC: bars]
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ int s_acc, s_bad, s_tok, s_cross_tile;
     __shared__ u64 s_cross_run;
@@ -114,8 +116,7 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
     const int tpc = (ntiles + kSpecCluster - 1) / kSpecCluster;  // tiles per CTA
     float* ring = reinterpret_cast<float*>(smem_raw);
     u64* tsum = reinterpret_cast<u64*>(smem_raw + (VEC ? kSpecRingBytes : 0));
-    u64* all = tsum + tpc;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(all + ntiles);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(tsum + tpc);
     if (VEC && tid == 0) {
         for (int i = 0; i < kSpecStages; ++i) mbar_init(bars + i, 1);
         mbar_fence_init();
@@ -247,27 +248,28 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
             for (int off = 16; off; off >>= 1) c += shfl_xor_u64(c, off);
             if (lane == 0) s_chunk = c;
         }
-        cluster.sync();  // every CTA's tile sums and share are visible cluster-wide
-        u64 total = 0;
-        for (int r = 0; r < kSpecCluster; ++r) total += *cluster.map_shared_rank(&s_chunk, r);
+        cluster.sync();  // every CTA's share is visible cluster-wide
+        u64 total = 0, before = 0;  // the row's sum, and the sum of the shares before this CTA's
+        for (int r = 0; r < kSpecCluster; ++r) {
+            const u64 v = *cluster.map_shared_rank(&s_chunk, r);
+            total += v;
+            if (r < rank) before += v;
+        }
         if (total == 0) {
             cluster.sync();  // nobody reads this attempt's sums any more
             if (acc == k) break;  // the target row itself is zero: no token
             continue;
         }
-        if (rank == 0) {
+        const u64 target = scaled_floor(a.u_res[b], total);
+        if (before <= target && target - before < s_chunk) {
+            // this CTA's share holds the crossing: scan its tile sums in runs, a run per thread
             if (tid == 0) s_cross_tile = -1;
-            for (int t = tid; t < ntiles; t += kSpecThreads) {
-                const int r = t / tpc;
-                all[t] = cluster.map_shared_rank(tsum, r)[t - r * tpc];
-            }
-            __syncthreads();
-            const u64 target = scaled_floor(a.u_res[b], total);
-            const int per = (ntiles + kSpecThreads - 1) / kSpecThreads;
+            const int nt = my1 - my0;
+            const int per = (nt + kSpecThreads - 1) / kSpecThreads;
             const int t0 = tid * per;
-            const int t1 = min(ntiles, t0 + per);
+            const int t1 = min(nt, t0 + per);
             u64 mine = 0;
-            for (int t = t0; t < t1; ++t) mine += all[t];
+            for (int t = t0; t < t1; ++t) mine += tsum[t];
             u64 incl = mine;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -276,18 +278,18 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
             }
             if (lane == 31) s_warp[warp] = incl;
             __syncthreads();
-            u64 before = 0;
-            for (int w = 0; w < warp; ++w) before += s_warp[w];
-            const u64 excl = before + incl - mine;
+            u64 bw = before;
+            for (int w = 0; w < warp; ++w) bw += s_warp[w];
+            const u64 excl = bw + incl - mine;
             if (excl <= target && target < excl + mine) {
                 // the crossing lies in this thread's run: find its tile from the sums
                 u64 run = excl;
                 int t = t0;
                 for (; t < t1 - 1; ++t) {
-                    if (run + all[t] > target) break;
-                    run += all[t];
+                    if (run + tsum[t] > target) break;
+                    run += tsum[t];
                 }
-                s_cross_tile = t;
+                s_cross_tile = my0 + t;
                 s_cross_run = run;
             }
             __syncthreads();
@@ -313,10 +315,10 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
                     if (hit < 0 && r > target) hit = (int)(x0 + j);
                 }
                 const unsigned m = __ballot_sync(0xffffffffu, hit >= 0);
-                if (m && lane == __ffs((int)m) - 1) s_tok = hit;
+                if (m && lane == __ffs((int)m) - 1) *cluster.map_shared_rank(&s_tok, 0) = hit;
             }
         }
-        cluster.sync();  // CTA 0 is done reading the others' shared memory
+        cluster.sync();  // the token is in CTA 0's shared memory; nobody reads the shares any more
         break;
     }
     if (rank == 0) {
@@ -335,7 +337,7 @@ size_t spec_smem_bytes(long long n) {
     const long long ntiles = (n + kSpecTile - 1) / kSpecTile;
     const long long tpc = (ntiles + kSpecCluster - 1) / kSpecCluster;
     const size_t ring = n % 4 == 0 ? kSpecRingBytes : 0;
-    return ring + (size_t)(tpc + ntiles) * sizeof(u64) + kSpecStages * sizeof(uint64_t);
+    return ring + (size_t)tpc * sizeof(u64) + kSpecStages * sizeof(uint64_t);
 }
 
 cudaError_t launch_spec_accept(const SpecArgs& a, cudaStream_t st) {
