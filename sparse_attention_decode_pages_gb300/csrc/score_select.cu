@@ -43,7 +43,7 @@ namespace spd {
 
 constexpr int kScoreWarps = 4;
 constexpr int kScoreThreads = 32 * kScoreWarps;
-constexpr int kScoreStages = 2;
+constexpr int kScoreStages = 2;  // (the slots' tile locations are kept in registers for exactly two)
 constexpr int kChunkTiles = 4;  // chained step: consecutive tiles a warp takes at a time
 constexpr int kTailTiles = 2;   // chained step: tiles per warp handed out singly at the end
 
@@ -821,9 +821,24 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
         p0 = (tb - 1 - (local - h * tb)) * 16;
     };
     int issued_row = -1;
+    // Each slot's tile as located at issue (read back when it is scored); a tile
+    // that continues the previously issued one's row is its 16 pages further down.
+    static_assert(kScoreStages == 2, "one register set per slot");
+    int4 loc_s0 = make_int4(0, 0, 0, 0), loc_s1 = make_int4(0, 0, 0, 0);
+    long long last_g = -2;
+    int4 last_loc = make_int4(0, 0, 0, 0);  // {b, h, p0, P}
     auto issue = [&](int t, long long g) {
-        int b, h, p0, P;
-        locate(g, b, h, p0, P);
+        if (g == last_g + 1 && last_loc.z >= 16) {
+            last_loc.z -= 16;
+        } else {
+            int b_, h_, p0_, P_;
+            locate(g, b_, h_, p0_, P_);
+            last_loc = make_int4(b_, h_, p0_, P_);
+        }
+        last_g = g;
+        const int b = last_loc.x, h = last_loc.y, p0 = last_loc.z, P = last_loc.w;
+        if (t % kScoreStages == 0) loc_s0 = last_loc;
+        else loc_s1 = last_loc;
         const int row = b * a.H_kv + h;
         const bool newq = row != issued_row;
         issued_row = row;
@@ -856,8 +871,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(ScoreSelect
         const int slot = t % kScoreStages;
         const long long g = gq[slot];
         if (g < 0) break;  // tiles are grabbed in order: every earlier one is done
-        int b, h, p0, P;
-        locate(g, b, h, p0, P);
+        const int4 loc = slot == 0 ? loc_s0 : loc_s1;
+        const int b = loc.x, h = loc.y, p0 = loc.z, P = loc.w;
         const int row = b * a.H_kv + h;
         if (!mbar_wait_bounded(bars + slot, (uint32_t)((t / kScoreStages) & 1), a.status, a.wait_ns)) {
             // Let the copies still in flight land (bounded) before giving up.
