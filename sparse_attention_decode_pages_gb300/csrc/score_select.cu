@@ -334,10 +334,15 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
             __nanosleep(64);
             missing = repoll_keys(kg, keys, P0, tid, NT);
         }
-        // acquire: the fused append's writes, released before its tile's keys, are
-        // visible from here on (and, through the publish below, to the attention)
-        fence_acq_rel_gpu();
-        for (int p = tid; p < P0; p += NT) kg[p] = 0u;  // zero again for the next call
+        // acquire: the fused append's writes are released before the keys of its tile
+        // (the row's last), so thread 0, which publishes the row below, reads the last
+        // key again with acquire semantics before it is zeroed: from then on the
+        // append is visible to it and, through its release, to the attention
+        if (tid == 0 && P0 > 0) {
+            (void)ld_acquire(kg + P0 - 1);
+            kg[P0 - 1] = 0u;
+        }
+        for (int p = tid; p < P0 - 1; p += NT) kg[p] = 0u;  // zero again for the next call
         if (tid == 0) a.tiles_done[row] = 0u;                     // this row's count is consumed
     }
     // chained step: the row's selection is published to the attention kernel
