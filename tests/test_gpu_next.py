@@ -544,6 +544,45 @@ def test_decode_step_wait_runs_out_and_the_next_call_is_clean():
         assert np.array_equal(x, y), what
 
 
+def test_decode_step_bad_page_id_sets_status_and_does_not_fault():
+    """A page-table entry outside the cache in the chained step (where the selection
+    hands the attention each selected page's physical page): the sink page of one
+    sequence, always selected, points past the last physical page.  The step sets
+    SPD_DEV_BAD_PAGE, skips that page, faults nowhere, and the other sequences get the
+    bits of a run on the good table; the next call on the good table is clean."""
+    import torch
+    import sparse_attention_decode_pages_gb300 as spd
+    w = wl.named("q17b", threads=8, B=16, len_lo=300, len_hi=1500,
+                 policy=wl.BudgetPolicy("fixed", fixed_pages=24, sink_pages=1, local_pages=4))
+
+    def run(page_table):
+        g = Gpu(w)
+        summ = g.summarize()
+        d = g.d
+        sel = torch.full((w.B, w.H_kv, w.k_max), -1, dtype=torch.int32, device="cuda")
+        nsel = torch.full((w.B, w.H_kv), -7, dtype=torch.int32, device="cuda")
+        o = torch.zeros((w.B, w.H_q, w.D), dtype=torch.bfloat16, device="cuda")
+        lse = torch.zeros((w.B, w.H_q), device="cuda")
+        ws = g.ws(spd.spd_sparse_decode_step_workspace_size(g.dims, w.k_max))
+        spd.sparse_decode_step(g.dims, d["K"], d["V"], page_table(d), d["seq_lens"], None, None, d["q"], summ,
+                               w.policy, sel, nsel, w.k_max, o, ws, lse=lse)
+        torch.cuda.synchronize()
+        return spd.spd_device_status(clear=True), _bits(o), lse.view(torch.int32).cpu().numpy()
+
+    def bad_table(d):
+        t = d["page_table"].clone()
+        t[3, 0] = w.num_phys_pages + 5
+        return t
+
+    st_bad, o_bad, lse_bad = run(bad_table)
+    assert st_bad == spd.DEV_BAD_PAGE, st_bad
+    st_good, o_good, lse_good = run(lambda d: d["page_table"])
+    assert st_good == 0, st_good
+    others = [b for b in range(w.B) if b != 3]
+    assert np.array_equal(o_bad[others], o_good[others])
+    assert np.array_equal(lse_bad[others], lse_good[others])
+
+
 def test_decode_step_ties_go_to_lower_pages():
     """Pages with identical keys score alike: the chained step takes the mandatory pages
     and then the lowest page ids, at 41 and at 100 pages per row."""
