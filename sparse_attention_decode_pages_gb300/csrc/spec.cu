@@ -96,6 +96,15 @@ __device__ __forceinline__ u64 shfl_xor_u64(u64 v, int off) {
     return __shfl_xor_sync(0xffffffffu, v, off);
 }
 
+// Warp sum of one tile's lane sums (each < 4 * 2^40 = 2^42): the low and the high 21
+// bits are summed separately, each by one warp-reduce instruction (32 lanes x 2^21 <
+// 2^26 fits 32 bits), so the 64-bit total is exact.
+__device__ __forceinline__ u64 tile_sum(u64 v) {
+    const unsigned lo = __reduce_add_sync(0xffffffffu, (unsigned)(v & 0x1fffffull));
+    const unsigned hi = __reduce_add_sync(0xffffffffu, (unsigned)(v >> 21));
+    return ((u64)hi << 21) + lo;
+}
+
 template <bool VEC>
 __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThreads, 4)
     spec_accept_kernel(SpecArgs a) {
@@ -203,8 +212,7 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
                         sum = spec_w(q4.x, p4.x, residual) + spec_w(q4.y, p4.y, residual) +
                               spec_w(q4.z, p4.z, residual) + spec_w(q4.w, p4.w, residual);
                     }
-#pragma unroll
-                    for (int off = 16; off; off >>= 1) sum += shfl_xor_u64(sum, off);
+                    sum = tile_sum(sum);
                     const int t = (int)((s0 - e0) / kSpecTile) + tw;
                     if (lane == 0 && t < my1 - my0) tsum[t] = sum;
                 }
@@ -234,8 +242,7 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
                     if (tt >= my1) break;  // warp-uniform
                     u64 sum = spec_w(q4[u].x, p4[u].x, residual) + spec_w(q4[u].y, p4[u].y, residual) +
                               spec_w(q4[u].z, p4[u].z, residual) + spec_w(q4[u].w, p4[u].w, residual);
-#pragma unroll
-                    for (int off = 16; off; off >>= 1) sum += shfl_xor_u64(sum, off);
+                    sum = tile_sum(sum);
                     if (lane == 0) tsum[tt - my0] = sum;
                 }
             }
