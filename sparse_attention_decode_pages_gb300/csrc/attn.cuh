@@ -782,60 +782,120 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
         consumers_sync();  // s_flag is reused by the next unit
         if (!last) continue;
         // Last unit of the row: merge the partials of this warp's rows.  Lane s
-        // holds split s's lse; each lane owns D/32 consecutive channels, and the
-        // loads of a split are independent of each other.
-        const long long rbase = (long long)cu.row * a.num_splits * R;
-        constexpr int DPL = D / 32;  // channels per lane
-        for (int r = mt * 16; r < min(R, mt * 16 + 16); ++r) {
-            float M = NEG_INF;
-            for (int s0 = 0; s0 < cu.nsplit; s0 += 32)
-                if (s0 + lane < cu.nsplit) M = fmaxf(M, __ldcg(a.part_lse + rbase + (long long)(s0 + lane) * R + r));
+        // holds split s's lse; each lane owns D/32 consecutive channels.
+        if constexpr (C::TRS && D == 128) {
+            // Per output row one L2 round trip for the lse of every split (loaded
+            // once, kept for the max, the sum and the weights), then one per batch
+            // of SB splits' o; each lane owns 4 channels.  (Issuing the first o
+            // batch with the lse saves one more round trip per row but made the
+            // page loop of this kernel measurably slower.)
+            constexpr int SB = 4;  // splits whose o loads are in flight together
+            const long long rbase = (long long)cu.row * a.num_splits * R;
+            const int ns = cu.nsplit;
+            for (int r = mt * 16; r < min(R, mt * 16 + 16); ++r) {
+                const float* lse_r = a.part_lse + rbase + r;                // split s: lse_r[s * R]
+                const float4* o_r = reinterpret_cast<const float4*>(a.part_o + (rbase + r) * D) + lane;
+                const long long o_step = (long long)R * D / 4;              // split s: o_r[s * o_step]
+                const float ls0 = lane < ns ? __ldcg(lse_r + (long long)lane * R) : NEG_INF;
+                float M = ls0;
+                for (int s = 32 + lane; s < ns; s += 32) M = fmaxf(M, __ldcg(lse_r + (long long)s * R));
 #pragma unroll
-            for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            float L = 0.f;
-            if (M != NEG_INF)
-                for (int s0 = 0; s0 < cu.nsplit; s0 += 32)
-                    if (s0 + lane < cu.nsplit) L += __expf(__ldcg(a.part_lse + rbase + (long long)(s0 + lane) * R + r) - M);
+                for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+                float L = 0.f;
+                if (M != NEG_INF) {
+                    if (lane < ns) L += __expf(ls0 - M);
+                    for (int s = 32 + lane; s < ns; s += 32) L += __expf(__ldcg(lse_r + (long long)s * R) - M);
+                }
 #pragma unroll
-            for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-            const float lse_all = M == NEG_INF ? NEG_INF : M + __logf(L);
-            float acc[DPL];
+                for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+                const float lse_all = M == NEG_INF ? NEG_INF : M + __logf(L);
+                const float wl0 = (lane < ns && ls0 != NEG_INF && M != NEG_INF) ? __expf(ls0 - lse_all) : 0.f;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (M != NEG_INF) {
+                    for (int s0 = 0; s0 < ns; s0 += SB) {
+                        float4 v[SB];
 #pragma unroll
-            for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-            if (M != NEG_INF) {
-                for (int s0 = 0; s0 < cu.nsplit; s0 += 32) {
-                    const int ns = min(32, cu.nsplit - s0);
-                    float wl = 0.f;
-                    if (lane < ns) {
-                        const float ls = __ldcg(a.part_lse + rbase + (long long)(s0 + lane) * R + r);
-                        wl = ls == NEG_INF ? 0.f : __expf(ls - lse_all);
-                    }
-#pragma unroll 4
-                    for (int k = 0; k < ns; ++k) {
-                        const float wk = __shfl_sync(0xffffffffu, wl, k);
-                        const float* src = a.part_o + (rbase + (long long)(s0 + k) * R + r) * D + lane * DPL;
-                        if (DPL == 4) {
-                            const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-                            acc[0] += wk * v.x;
-                            acc[1 % DPL] += wk * v.y;
-                            acc[2 % DPL] += wk * v.z;
-                            acc[3 % DPL] += wk * v.w;
-                        } else {
-                            const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
-                            acc[0] += wk * v.x;
-                            acc[1 % DPL] += wk * v.y;
+                        for (int k = 0; k < SB; ++k)
+                            if (s0 + k < ns) v[k] = __ldcg(o_r + (s0 + k) * o_step);
+#pragma unroll
+                        for (int k = 0; k < SB; ++k) {
+                            const int s = s0 + k;
+                            if (s >= ns) break;
+                            float wk;
+                            if (s < 32) {
+                                wk = __shfl_sync(0xffffffffu, wl0, s);
+                            } else {
+                                const float ls = __ldcg(lse_r + (long long)s * R);
+                                wk = ls == NEG_INF ? 0.f : __expf(ls - lse_all);
+                            }
+                            acc.x += wk * v[k].x;
+                            acc.y += wk * v[k].y;
+                            acc.z += wk * v[k].z;
+                            acc.w += wk * v[k].w;
                         }
                     }
                 }
+                const long long oi = out_index(cu.row, r);
+                *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(a.o) + oi * D + lane * 4) =
+                    make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+                if (lane == 0 && a.lse) a.lse[oi] = lse_all;
             }
-            const long long oi = out_index(cu.row, r);
-            bf16* dst = reinterpret_cast<bf16*>(a.o) + oi * D + lane * DPL;
-            if (DPL == 4) {
-                *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(acc[0], acc[1 % DPL]), pack_bf16(acc[2 % DPL], acc[3 % DPL]));
-            } else {
-                *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0], acc[1 % DPL]);
+        } else {
+            // The lse is read per phase (max, sum, weights) and the o loads of a
+            // split are independent of each other.
+            const long long rbase = (long long)cu.row * a.num_splits * R;
+            constexpr int DPL = D / 32;  // channels per lane
+            for (int r = mt * 16; r < min(R, mt * 16 + 16); ++r) {
+                float M = NEG_INF;
+                for (int s0 = 0; s0 < cu.nsplit; s0 += 32)
+                    if (s0 + lane < cu.nsplit) M = fmaxf(M, __ldcg(a.part_lse + rbase + (long long)(s0 + lane) * R + r));
+#pragma unroll
+                for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+                float L = 0.f;
+                if (M != NEG_INF)
+                    for (int s0 = 0; s0 < cu.nsplit; s0 += 32)
+                        if (s0 + lane < cu.nsplit) L += __expf(__ldcg(a.part_lse + rbase + (long long)(s0 + lane) * R + r) - M);
+#pragma unroll
+                for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+                const float lse_all = M == NEG_INF ? NEG_INF : M + __logf(L);
+                float acc[DPL];
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+                if (M != NEG_INF) {
+                    for (int s0 = 0; s0 < cu.nsplit; s0 += 32) {
+                        const int ns = min(32, cu.nsplit - s0);
+                        float wl = 0.f;
+                        if (lane < ns) {
+                            const float ls = __ldcg(a.part_lse + rbase + (long long)(s0 + lane) * R + r);
+                            wl = ls == NEG_INF ? 0.f : __expf(ls - lse_all);
+                        }
+#pragma unroll 4
+                        for (int k = 0; k < ns; ++k) {
+                            const float wk = __shfl_sync(0xffffffffu, wl, k);
+                            const float* src = a.part_o + (rbase + (long long)(s0 + k) * R + r) * D + lane * DPL;
+                            if (DPL == 4) {
+                                const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+                                acc[0] += wk * v.x;
+                                acc[1 % DPL] += wk * v.y;
+                                acc[2 % DPL] += wk * v.z;
+                                acc[3 % DPL] += wk * v.w;
+                            } else {
+                                const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+                                acc[0] += wk * v.x;
+                                acc[1 % DPL] += wk * v.y;
+                            }
+                        }
+                    }
+                }
+                const long long oi = out_index(cu.row, r);
+                bf16* dst = reinterpret_cast<bf16*>(a.o) + oi * D + lane * DPL;
+                if (DPL == 4) {
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(acc[0], acc[1 % DPL]), pack_bf16(acc[2 % DPL], acc[3 % DPL]));
+                } else {
+                    *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0], acc[1 % DPL]);
+                }
+                if (lane == 0 && a.lse) a.lse[oi] = lse_all;
             }
-            if (lane == 0 && a.lse) a.lse[oi] = lse_all;
         }
         if (tid == 0) a.counters[cu.row] = 0;
     }

@@ -66,12 +66,16 @@ __device__ __forceinline__ long long budget_pages(const spd_budget_policy& pol, 
     return (len * pol.frac_num + pol.frac_den * ps - 1) / (pol.frac_den * ps);
 }
 
-// Selection CTAs: 256 threads for one row after the scoring grid, 128 in the
-// chained step (two per SM fit beside the three scoring CTAs).  Once the radix
-// digit being refined holds at most NT candidates, they are ranked directly
-// (pairwise, a thread each) instead of refining further digits.
+// Selection CTAs: 256 threads for one row after the scoring grid.  In the
+// chained step the width follows the row count: 128 threads, two per SM beside
+// the three scoring CTAs, when there are more rows than two per SM (the rows
+// become ready over the scoring and their selection overlaps it); 256 threads
+// for up to two rows per SM and 512 for up to one (few long rows, all ready at
+// about the same time, with nothing else to overlap their selection).  Once the
+// radix digit being refined holds at most kRankMax candidates, they are ranked
+// directly (pairwise, a thread each) instead of refining further digits.
 constexpr int kSelThreads = 256;
-constexpr int kSelThreadsChained = 128;
+constexpr int kRankMax = 128;
 
 __device__ __forceinline__ float key_float(uint32_t u) {
     return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
@@ -285,8 +289,9 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
     __shared__ int s_digit, s_rem, s_cnt, s_ncol;
     __shared__ uint32_t s_kmin, s_kmax;
     __shared__ int w_eq[NWARP], w_take[NWARP];
-    __shared__ uint32_t col_key[NT];
-    __shared__ int col_p[NT];
+    constexpr int RK = NT < kRankMax ? NT : kRankMax;  // candidates ranked directly
+    __shared__ uint32_t col_key[RK];
+    __shared__ int col_p[RK];
     // after the keys: boundary pages chosen by rank and the final decision (a bit
     // per page each), (top-p) the page weights, (chained step) the row's page table
     const int words = (a.max_pages + 31) / 32;
@@ -437,13 +442,13 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
         // The bits above h are the same in every candidate (their minimum and maximum
         // agree there): the radix starts below them, so the first digit already
         // spreads the keys.  Digits of up to 8 bits until the boundary digit holds at
-        // most NT keys (then ranked) or every bit is refined (an exact key).
+        // most RK keys (then ranked) or every bit is refined (an exact key).
         int h = 31 - __clz((int)(s_kmin ^ s_kmax));  // -1 when all candidates are equal
         pmask = h < 0 ? 0xffffffffu : (h >= 31 ? 0u : ~((2u << h) - 1u));
         prefix = s_kmin & pmask;
         int ncnt = ncand;
         bool clean = a.pol.mode != SPD_BUDGET_TOP_P;  // the first level's histogram is clear
-        while (h >= 0 && ncnt > NT) {
+        while (h >= 0 && ncnt > RK) {
             const int wd = h + 1 < 8 ? h + 1 : 8;
             const int shift = h + 1 - wd;
             const uint32_t dmask = (1u << wd) - 1u;
@@ -505,7 +510,7 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
             ncnt = s_cnt;
             h = shift - 1;
         }
-        ranked = ncnt <= NT;  // block-uniform
+        ranked = ncnt <= RK;  // block-uniform
         thr = prefix;
     }
     if (ranked) {
@@ -521,7 +526,7 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
             if (bm && lane == 0) base = atomicAdd(&s_ncol, __popc(bm));  // one atomic per warp
             base = __shfl_sync(0xffffffffu, base, 0);
             if (in) {
-                const int at = base + __popc(bm & lt_mask);  // < s_cnt <= NT
+                const int at = base + __popc(bm & lt_mask);  // < s_cnt <= RK
                 col_key[at] = u;
                 col_p[at] = p;
             }
@@ -992,13 +997,18 @@ cudaError_t launch_score_select(const ScoreSelectArgs& a, int num_sms, cudaStrea
                          (a.sel_phys ? (size_t)a.max_pages : 0)) * sizeof(uint32_t);
     long long sgrid = (long long)a.B * a.H_kv;
     if (a.tiles_done) {
-        // chained step: two 128-thread CTAs per SM, resident beside the scoring CTAs
-        // from the start (so the attention grid is launched early), rows in order
-        auto kern = select_kernel<kSelThreadsChained>;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        if (sgrid > 2LL * num_sms) sgrid = 2LL * num_sms;
-        return launch_pdl(kern, dim3((unsigned)sgrid), dim3(kSelThreadsChained), smem, st, a);
+        // chained step: persistent CTAs taking the rows in order, launched right
+        // behind the scoring grid (so the attention grid is launched early); the
+        // width by row count (above)
+        auto chained = [&](auto kern, int nt, long long per_sm) -> cudaError_t {
+            cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e2 != cudaSuccess) return e2;
+            if (sgrid > per_sm * num_sms) sgrid = per_sm * num_sms;
+            return launch_pdl(kern, dim3((unsigned)sgrid), dim3(nt), smem, st, a);
+        };
+        if (sgrid <= num_sms) return chained(select_kernel<512>, 512, 1);
+        if (sgrid <= 2LL * num_sms) return chained(select_kernel<256>, 256, 2);
+        return chained(select_kernel<128>, 128, 2);
     }
     auto kern = select_kernel<kSelThreads>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
