@@ -20,13 +20,20 @@
 // The draw streams the row once.  Each CTA sums the 128-element tiles of its
 // share of the row into its shared memory: rows whose length is a multiple of
 // 4 arrive through a 3-deep ring of 16-tile chunks filled by bulk copies (each
-// warp sums two tiles of each chunk); other rows through plain loads, a warp
-// per tile.  Eight 8-warp CTAs per sequence fit in one wave at B = 64.  After a
+// warp reads two tiles of each chunk into registers, frees the slot, then sums
+// them); other rows through plain loads, a warp per tile.  Eight 8-warp CTAs per sequence fit in one wave at B = 64.  After a
 // cluster barrier every CTA reads the eight shares' sums through distributed
 // shared memory; the one CTA whose share holds the target block-scans its own
 // tile sums, the one thread whose run of tiles holds it finds the crossing
-// tile, a warp scans that tile's 128 weights to find the element, and the
-// token goes to CTA 0, which writes the outputs.
+// tile, and a warp scans that tile's 128 weights to find the element and
+// writes the token (CTA 0 has written the other outputs at the start).  The
+// barrier after the shares are read is split: each CTA arrives once it has read
+// them and waits only before its own shared memory is rewritten or released, so
+// the search holds no other CTA back.
+//
+// Most tiles hold only probabilities below 2^-10, whose grid values fit 30 bits:
+// their weights are formed and summed in 32-bit arithmetic (a float-to-uint32
+// conversion of v * 2^40), the rest in the exact 64-bit form below.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -42,9 +49,10 @@ constexpr int kSpecCluster = 8;
 constexpr int kSpecUnroll = 2;
 // n % 4 == 0 rows stream through shared memory: chunks of 16 tiles (q and p),
 // kSpecStages in flight per CTA, copied by the bulk-copy engine.
-constexpr int kSpecChunk = 16 * kSpecTile;  // elements
+constexpr int kSpecChunk = 16 * kSpecTile;  // elements (a whole number of tiles per warp)
 constexpr int kSpecStages = 3;
 constexpr size_t kSpecRingBytes = (size_t)kSpecStages * 2 * kSpecChunk * sizeof(float);
+static_assert(kSpecChunk / kSpecTile % (kSpecThreads / 32) == 0, "every warp sums the same number of tiles of a chunk");
 typedef unsigned long long u64;
 
 // floor(2^40 v) from the float's bits, in integer operations only (a 64-bit
@@ -63,6 +71,28 @@ __device__ __forceinline__ u64 fixed40(float v) {
         w = one ? (1ull << 40) : 0ull;
     }
     return w;
+}
+
+// floor(2^40 v) when it lies below 2^32: v * 2^40 is exact in fp32 (a power-of-two
+// scaling that neither overflows nor leaves the normal range for a normal v below 2^-8),
+// and the float-to-uint32 conversion truncates it, i.e. floors it.  The conversion
+// saturates: 0 for a negative v or a NaN (as fixed40), 2^32 - 1 for a v of 2^-8 or more
+// or +inf, so a result below 2^30 is always the exact floor(2^40 v).
+__device__ __forceinline__ unsigned fixed40_u32(float v) { return __float2uint_rz(v * 1099511627776.0f); }
+
+// The four weights of a lane's float4 pair in 32-bit arithmetic, and whether they are
+// exact and their sum fits 32 bits (every converted value below 2^30).
+__device__ __forceinline__ bool spec_w4_small(const float4& q4, const float4& p4, bool residual, unsigned& sum) {
+    unsigned w[4] = {fixed40_u32(q4.x), fixed40_u32(q4.y), fixed40_u32(q4.z), fixed40_u32(q4.w)};
+    unsigned any = w[0] | w[1] | w[2] | w[3];
+    if (residual) {
+        const unsigned v[4] = {fixed40_u32(p4.x), fixed40_u32(p4.y), fixed40_u32(p4.z), fixed40_u32(p4.w)};
+        any |= v[0] | v[1] | v[2] | v[3];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = max(w[i], v[i]) - v[i];
+    }
+    sum = w[0] + w[1] + w[2] + w[3];
+    return any < (1u << 30);
 }
 
 __device__ __forceinline__ u64 spec_w(float qv, float pv, bool residual) {
@@ -110,7 +140,7 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
     spec_accept_kernel(SpecArgs a) {
     // [VEC: ring of kSpecStages x {q, p} chunks][tpc own tile sums][VEC: bars]
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    __shared__ int s_acc, s_bad, s_tok, s_cross_tile;
+    __shared__ int s_acc, s_bad, s_cross_tile;
     __shared__ u64 s_cross_run;
     __shared__ u64 s_warp[kSpecThreads / 32];
     __shared__ u64 s_chunk;  // this CTA's share of the total
@@ -156,7 +186,6 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
             // a bad token at the first failing position invalidates the sequence
             s_acc = j;
             s_bad = (j < k && ((badm >> j) & 1u)) ? 1 : 0;
-            s_tok = -1;
             if (s_bad && rank == 0) raise_status(a.status, SPD_DEV_BAD_TOKEN);
         }
     }
@@ -169,6 +198,12 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
             if (tid == 0) a.n_accepted[b] = 0;
         }
         return;
+    }
+    // CTA 0 writes the outputs now, the drawn token's slot as "none"; the CTA that finds
+    // the token overwrites that slot (ordered after this write by the cluster barrier)
+    if (rank == 0) {
+        for (int i = tid; i <= k; i += kSpecThreads) out[i] = i < acc ? a.draft[(long long)b * k + i] : -1;
+        if (tid == 0) a.n_accepted[b] = acc;
     }
     const float* qr = a.q + ((long long)b * (k + 1) + acc) * n;
     const float* pr = acc < k ? a.p + ((long long)b * k + acc) * n : qr;
@@ -198,26 +233,40 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
                 const int slot = (int)((chunks_done + c) % kSpecStages);
                 if (!dead && !mbar_wait_bounded(bars + slot, ((chunks_done + c) / kSpecStages) & 1u, a.status, a.wait_ns))
                     dead = true;
-                // warp w sums tiles w, w + NW, ... of the chunk
+                // warp w sums tiles w, w + NW, ... of the chunk: their values are read
+                // into registers first, so the slot is refilled while they are summed
+                constexpr int TPW = kSpecChunk / kSpecTile / NW;  // tiles per warp
                 const long long s0 = e0 + (long long)c * kSpecChunk;
+                float4 q4[TPW], p4[TPW];
 #pragma unroll
-                for (int tw = warp; tw < kSpecChunk / kSpecTile; tw += NW) {
+                for (int u = 0; u < TPW; ++u) {
+                    const int tw = warp + u * NW;
                     const long long x0 = s0 + (long long)tw * kSpecTile + lane * 4;
-                    u64 sum = 0;
+                    q4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    p4[u] = q4[u];
                     if (!dead && x0 < e1) {
                         const float* src = ring + (size_t)slot * 2 * kSpecChunk + tw * kSpecTile + lane * 4;
-                        const float4 q4 = *reinterpret_cast<const float4*>(src);
-                        const float4 p4 = residual ? *reinterpret_cast<const float4*>(src + kSpecChunk)
-                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-                        sum = spec_w(q4.x, p4.x, residual) + spec_w(q4.y, p4.y, residual) +
-                              spec_w(q4.z, p4.z, residual) + spec_w(q4.w, p4.w, residual);
+                        q4[u] = *reinterpret_cast<const float4*>(src);
+                        if (residual) p4[u] = *reinterpret_cast<const float4*>(src + kSpecChunk);
                     }
-                    sum = tile_sum(sum);
-                    const int t = (int)((s0 - e0) / kSpecTile) + tw;
-                    if (lane == 0 && t < my1 - my0) tsum[t] = sum;
                 }
                 __syncthreads();  // the slot has been read
                 if (tid == 0 && c + kSpecStages < nchunks) issue(c + kSpecStages);
+#pragma unroll
+                for (int u = 0; u < TPW; ++u) {
+                    // a tile of small values (the usual case) in 32-bit operations, others in 64
+                    u64 sum;
+                    unsigned s32;
+                    if (__all_sync(0xffffffffu, spec_w4_small(q4[u], p4[u], residual, s32))) {
+                        sum = s32;
+                    } else {
+                        sum = spec_w(q4[u].x, p4[u].x, residual) + spec_w(q4[u].y, p4[u].y, residual) +
+                              spec_w(q4[u].z, p4[u].z, residual) + spec_w(q4[u].w, p4[u].w, residual);
+                    }
+                    sum = tile_sum(sum);
+                    const int t = (int)((s0 - e0) / kSpecTile) + warp + u * NW;
+                    if (lane == 0 && t < my1 - my0) tsum[t] = sum;
+                }
             }
             chunks_done += nchunks;
         } else {
@@ -262,8 +311,11 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
             total += v;
             if (r < rank) before += v;
         }
+        // done with the other CTAs' shared memory: arrive now, wait before this CTA's
+        // shared memory is rewritten or released (so the search below holds nobody back)
+        asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
         if (total == 0) {
-            cluster.sync();  // nobody reads this attempt's sums any more
+            asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
             if (acc == k) break;  // the target row itself is zero: no token
             continue;
         }
@@ -322,21 +374,11 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
                     if (hit < 0 && r > target) hit = (int)(x0 + j);
                 }
                 const unsigned m = __ballot_sync(0xffffffffu, hit >= 0);
-                if (m && lane == __ffs((int)m) - 1) *cluster.map_shared_rank(&s_tok, 0) = hit;
+                if (m && lane == __ffs((int)m) - 1) out[acc] = hit;
             }
         }
-        cluster.sync();  // the token is in CTA 0's shared memory; nobody reads the shares any more
+        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // nobody reads the shares any more
         break;
-    }
-    if (rank == 0) {
-        __syncthreads();
-        for (int i = tid; i <= k; i += kSpecThreads) {
-            if (i < acc)
-                out[i] = a.draft[(long long)b * k + i];
-            else
-                out[i] = (i == acc) ? s_tok : -1;
-        }
-        if (tid == 0) a.n_accepted[b] = acc;
     }
 }
 

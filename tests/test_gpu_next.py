@@ -213,6 +213,78 @@ def test_spec_accept_all_accepted_zero_residual_and_empty_rows():
     assert tk_g[2, k] == -1 and tk_g[3, 0] == -1
 
 
+def _grid_row_mixed(n, rng):
+    """A residual row (p, q) whose grid weights W = max(0, floor(2^40 q) - floor(2^40 p))
+    are known exactly: most tiles hold only values below 2^-10 (the kernel's 32-bit
+    form), a few also hold values of 2^-10 and above, negative residuals and
+    subnormals (its 64-bit form).  The total stays below 2^23, so a float32 u can
+    place the draw's threshold on any integer."""
+    g = 2.0 ** -40
+    p = np.zeros(n, np.float64)
+    q = np.zeros(n, np.float64)
+    tiles = n // 128
+    wide = set(rng.choice(tiles, size=max(3, tiles // 6), replace=False).tolist())
+    for t in range(tiles):
+        base = t * 128
+        xs = rng.choice(128, size=40, replace=False) + base
+        for x in xs[:24]:                                   # tiny: W = m
+            q[x] = int(rng.integers(1, 3000)) * g
+        for x in xs[24:30]:                                 # just below 2^-10: W = 64 j
+            v = 2.0 ** -10 - int(rng.integers(1, 50)) * 2.0 ** -34
+            q[x], p[x] = v, v - int(rng.integers(1, 40)) * 2.0 ** -34
+        q[xs[30]] = 2.0 ** -140                             # subnormal: W = 0
+        if t in wide:
+            q[xs[31]], p[xs[31]] = 2.0 ** -10 + 2.0 ** -33, 2.0 ** -10           # W = 128
+            q[xs[32]], p[xs[32]] = 2.0 ** -9, 2.0 ** -9 - 3 * 2.0 ** -33         # W = 384
+            q[xs[33]], p[xs[33]] = 0.25 + int(rng.integers(1, 4)) * 2.0 ** -24, 0.25   # W = 2^16 j
+            q[xs[34]], p[xs[34]] = 0.5, 0.5 + 2.0 ** -24                       # residual < 0: W = 0
+            q[xs[35]], p[xs[35]] = 2.0 ** -10, 2.0 ** -10                     # W = 0 at the bound
+    p32, q32 = p.astype(np.float32), q.astype(np.float32)
+    assert np.array_equal(p32.astype(np.float64), p) and np.array_equal(q32.astype(np.float64), q)
+    F = lambda v: int(np.floor(np.ldexp(float(v), 40))) if v > 0 else 0
+    W = [max(0, F(qq) - F(pp)) for qq, pp in zip(q32.tolist(), p32.tolist())]
+    return p32, q32, W
+
+
+def test_spec_accept_grid_sums_exact_in_32_and_64_bit_tiles():
+    """The draw's running sums are exact on the 2^-40 grid in both of the kernel's
+    forms of a tile: thresholds on either side of running-sum boundaries spread
+    over every tile, where one grid step of error anywhere before the boundary
+    moves the token.  (The kernel's documented arithmetic, as in the grid cases.)"""
+    from fractions import Fraction
+    rng = np.random.default_rng(2024)
+    n, k = 4096, 2
+    p0, q0, W = _grid_row_mixed(n, rng)
+    C = np.cumsum(np.array(W, dtype=np.int64))
+    total = int(C[-1])
+    assert 0 < total < 2 ** 23
+    nz = [x for x in range(n) if W[x] > 0]
+    picks = [nz[i] for i in np.linspace(1, len(nz) - 1, 24).astype(int)]
+    thresholds, expect = [], []
+    for x in picks:
+        for T in (int(C[x - 1]), int(C[x]) - 1):   # both draw x
+            thresholds.append(T)
+            expect.append(x)
+    B = len(thresholds)
+    u = []
+    for T in thresholds:
+        f = np.float32(float(Fraction(2 * T + 1, 2 * total)))
+        while int(Fraction(float(f)) * total) > T:
+            f = np.nextafter(f, np.float32(0))
+        while int(Fraction(float(f)) * total) < T:
+            f = np.nextafter(f, np.float32(1))
+        assert int(Fraction(float(f)) * total) == T
+        u.append(f)
+    zero = [x for x in range(n) if p0[x] == 0 and q0[x] == 0][0]   # rejected: u_acc * 0 < 0 fails
+    p = np.broadcast_to(p0, (B, k, n)).copy()
+    q = np.broadcast_to(q0, (B, k + 1, n)).copy()
+    draft = np.full((B, k), zero, np.int32)
+    na, tk, st = _spec_gpu(p, q, draft, np.full((B, k), 0.5, np.float32), np.array(u, np.float32))
+    assert st == 0 and np.all(na == 0)
+    assert tk[:, 0].tolist() == expect
+    assert np.all(tk[:, 1:] == -1)
+
+
 def test_spec_accept_bad_draft_token_sets_status():
     d = wl.spec_inputs(B=3, k=2, n=512, seed=3)
     d["draft"][1, 1] = 512
