@@ -55,25 +55,34 @@ __global__ void __launch_bounds__(256) append_refresh_kernel(AppendArgs a) {
             mn[i] = pinf;
             mx[i] = ninf;
         }
-#pragma unroll 2
-        for (int t = r0; t < valid; t += RPI) {
-            const int pos = p * a.ps + t;
-            uint4 k;
-            if (pos >= first) {
-                const long long src = (((long long)b * a.T + (pos - first)) * a.H_kv + h) * (D / 8);
-                k = __ldg(reinterpret_cast<const uint4*>(a.k_new) + src + ch);
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.v_new) + src + ch);
-                kt[t * LPR + ch] = k;
-                vt[t * LPR + ch] = v;
-            } else {
-                k = kt[t * LPR + ch];
-            }
+        auto fold = [&](const uint4& k) {
             const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&k);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 mn[i] = __hmin2(mn[i], e[i]);
                 mx[i] = __hmax2(mx[i], e[i]);
             }
+        };
+        // rows t = r0, r0 + RPI, ... in order: the page's older rows (before the first
+        // new token) with kAppendBatch loads in flight, then the new ones, which are
+        // read from k_new / v_new and stored into the cache
+        const int nold = min(valid, max(0, first - p * a.ps));
+        for (int t0 = r0; t0 < nold; t0 += kAppendBatch * RPI) {
+            uint4 kk[kAppendBatch];
+#pragma unroll
+            for (int u = 0; u < kAppendBatch; ++u)
+                if (t0 + u * RPI < nold) kk[u] = kt[(t0 + u * RPI) * LPR + ch];
+#pragma unroll
+            for (int u = 0; u < kAppendBatch; ++u)
+                if (t0 + u * RPI < nold) fold(kk[u]);
+        }
+        for (int t = nold + ((r0 - nold) % RPI + RPI) % RPI; t < valid; t += RPI) {
+            const long long src = (((long long)b * a.T + (p * a.ps + t - first)) * a.H_kv + h) * (D / 8);
+            const uint4 k = __ldg(reinterpret_cast<const uint4*>(a.k_new) + src + ch);
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.v_new) + src + ch);
+            kt[t * LPR + ch] = k;
+            vt[t * LPR + ch] = v;
+            fold(k);
         }
 #pragma unroll
         for (int off = LPR; off < 32; off <<= 1) {

@@ -16,6 +16,12 @@ typedef __nv_bfloat16 bf16;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// Rows of a page whose key loads an appending warp keeps in flight at once when it
+// rebuilds the page's summary (one round trip per batch instead of per row): the
+// append kernel, and the scoring kernel's fused append (fewer there: its registers
+// decide how many scoring and selection CTAs share an SM).
+constexpr int kAppendBatch = 8;
+constexpr int kFusedAppendBatch = 4;
 
 // Every wait gives up after `limit` nanoseconds of the global timer (a launch
 // argument: spd_set_wait_limit_ns, 2 s by default), records SPD_DEV_TIMEOUT and

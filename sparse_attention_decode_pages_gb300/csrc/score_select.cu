@@ -662,23 +662,33 @@ __device__ void append_last_page(const ScoreSelectArgs& a, int b, int h, int len
         mn[i] = pinf;
         mx[i] = ninf;
     }
-    for (int t = r0; t < valid; t += RPI) {
-        uint4 k;
-        if (t == valid - 1) {
-            const long long src = ((long long)b * a.H_kv + h) * (D / 8);
-            k = __ldg(reinterpret_cast<const uint4*>(a.k_new) + src + ch);
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.v_new) + src + ch);
-            kt[t * LPR + ch] = k;
-            vt[t * LPR + ch] = v;
-        } else {
-            k = kt[t * LPR + ch];
-        }
+    auto fold = [&](const uint4& k) {
         const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&k);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             mn[i] = __hmin2(mn[i], e[i]);
             mx[i] = __hmax2(mx[i], e[i]);
         }
+    };
+    // rows t = r0, r0 + RPI, ... in order: the older ones with kFusedAppendBatch loads
+    // in flight, then (in its lanes) the new token's row, the page's last
+    const int last = valid - 1;
+    for (int t0 = r0; t0 < last; t0 += kFusedAppendBatch * RPI) {
+        uint4 kk[kFusedAppendBatch];
+#pragma unroll
+        for (int u = 0; u < kFusedAppendBatch; ++u)
+            if (t0 + u * RPI < last) kk[u] = kt[(t0 + u * RPI) * LPR + ch];
+#pragma unroll
+        for (int u = 0; u < kFusedAppendBatch; ++u)
+            if (t0 + u * RPI < last) fold(kk[u]);
+    }
+    if (r0 == last % RPI) {
+        const long long src = ((long long)b * a.H_kv + h) * (D / 8);
+        const uint4 k = __ldg(reinterpret_cast<const uint4*>(a.k_new) + src + ch);
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.v_new) + src + ch);
+        kt[last * LPR + ch] = k;
+        vt[last * LPR + ch] = v;
+        fold(k);
     }
 #pragma unroll
     for (int off = LPR; off < 32; off <<= 1) {
