@@ -52,9 +52,11 @@ template <int D, int PS, int NMT, bool SPARSE, int KS>
 struct AttnCfg {
     static constexpr int TILE = PS * D * 2;  // bytes of one K (or V) tile
     static constexpr int SLOT = 2 * TILE;
-    // ring depth: ~32-64 KB of K/V in flight per worker, a multiple of KS
+    // ring depth: ~32-128 KB of K/V in flight per worker, a multiple of KS (two slots
+    // per consumer group up to 32 KB slots: a group with one slot computes while
+    // nothing lands for it)
     static constexpr int STAGES = KS == 1 ? (SLOT <= 8192 ? 4 : (SLOT <= 16384 ? 3 : 2))
-                                          : (SLOT <= 16384 ? 2 * KS : KS);
+                                          : (SLOT <= 32768 ? 2 * KS : KS);
     static constexpr int CONSUMERS = NMT * KS;            // KS groups of NMT warps
     static constexpr int THREADS = (CONSUMERS + 1) * 32;  // consumers + one producer warp
     static constexpr int RP = NMT * 16;                   // padded rows
