@@ -21,8 +21,10 @@
 // share of the row into its shared memory: rows whose length is a multiple of
 // 4 arrive through a 3-deep ring of 16-tile chunks filled by bulk copies (each
 // warp reads two tiles of each chunk into registers, frees the slot, then sums
-// them); other rows through plain loads, a warp per tile.  Eight 8-warp CTAs per sequence fit in one wave at B = 64.  After a
-// cluster barrier every CTA reads the eight shares' sums through distributed
+// them); other rows through plain loads, a warp per tile.  Six 8-warp CTAs per
+// sequence: at B = 64 the 384 CTAs spread over every SM, two or three each (with
+// eight per sequence, four deep, they filled only ~128 SMs and took 8 % longer).
+// After a cluster barrier every CTA reads the six shares' sums through distributed
 // shared memory; the one CTA whose share holds the target block-scans its own
 // tile sums, the one thread whose run of tiles holds it finds the crossing
 // tile, and a warp scans that tile's 128 weights to find the element and
@@ -45,7 +47,7 @@ namespace spd {
 
 constexpr int kSpecThreads = 256;
 constexpr int kSpecTile = 128;
-constexpr int kSpecCluster = 8;
+constexpr int kSpecCluster = 6;
 constexpr int kSpecUnroll = 2;
 // n % 4 == 0 rows stream through shared memory: chunks of 16 tiles (q and p),
 // kSpecStages in flight per CTA, copied by the bulk-copy engine.
@@ -136,7 +138,7 @@ __device__ __forceinline__ u64 tile_sum(u64 v) {
 }
 
 template <bool VEC>
-__global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThreads, 4)
+__global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThreads, 3)
     spec_accept_kernel(SpecArgs a) {
     // [VEC: ring of kSpecStages x {q, p} chunks][tpc own tile sums][VEC: bars]
     extern __shared__ __align__(16) uint8_t smem_raw[];
