@@ -244,10 +244,10 @@ __device__ int top_p_pages(const ScoreSelectArgs& a, const uint32_t* keys, int P
 
 // Chained step: copies the row's P keys from global (kg) into shared memory (ks),
 // thread `me` of `NT` taking every NT-th key; the loads of a batch are issued
-// back to back before any is used.  True if this thread saw a key still 0 (not
-// yet written by the scoring).
-template <int NT>
-__device__ __forceinline__ bool gather_keys(const unsigned* kg, uint32_t* ks, int P, int me) {
+// back to back before any is used, and note(p, key) sees each key that is there.
+// True if this thread saw a key still 0 (not yet written by the scoring).
+template <int NT, class Note>
+__device__ __forceinline__ bool gather_keys(const unsigned* kg, uint32_t* ks, int P, int me, Note note) {
     constexpr int BATCH = 8;
     bool missing = false;
     for (int p0 = 0; p0 < P; p0 += NT * BATCH) {
@@ -260,20 +260,26 @@ __device__ __forceinline__ bool gather_keys(const unsigned* kg, uint32_t* ks, in
 #pragma unroll
         for (int i = 0; i < BATCH; ++i) {
             const int p = p0 + i * NT + me;
-            if (p < P) ks[p] = u[i];
+            if (p < P) {
+                ks[p] = u[i];
+                if (u[i] != 0u) note(p, u[i]);
+            }
             missing |= (u[i] == 0u);
         }
     }
     return missing;
 }
 
-// Reads again the keys still 0 in shared memory; true if one still is.
-__device__ __forceinline__ bool repoll_keys(const unsigned* kg, uint32_t* ks, int P, int me, int nt) {
+// Reads again the keys still 0 in shared memory (note(p, key) for each that has
+// arrived); true if one still is.
+template <class Note>
+__device__ __forceinline__ bool repoll_keys(const unsigned* kg, uint32_t* ks, int P, int me, int nt, Note note) {
     bool missing = false;
     for (int p = me; p < P; p += nt) {
         if (ks[p] == 0u) {
             const unsigned u = ld_relaxed(kg + p);
             ks[p] = u;
+            if (u != 0u) note(p, u);
             missing |= (u == 0u);
         }
     }
@@ -313,11 +319,25 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
     }
     for (int i = tid; i < 256; i += NT) hist[i] = 0;
     for (int w = tid; w < words; w += NT) s_chosen[w] = 0u;
+    const int P = max(0, seq_pages(len, a.ps, a.max_pages));  // a bad length: empty (flagged by the scoring)
+    const int sink = min(a.pol.sink_pages, P), local = min(a.pol.local_pages, P);
+    const int nm = min(P, sink + local);
+    const int ncand = P - nm;
+    auto mand = [&](int p) { return p < sink || p >= P - local; };
+    // the candidates' smallest and largest key (in the chained step taken while the
+    // keys are gathered)
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    auto note = [&](int p, uint32_t u) {
+        if (!mand(p)) {
+            kmin = min(kmin, u);
+            kmax = max(kmax, u);
+        }
+    };
     if (a.keys) {
         // chained step: wait for this row's tiles only, not for the whole scoring grid.
         // The count is a hint (an unordered add); each key is its own ready flag, so
         // the keys are gathered into shared memory and any still 0 is read again.
-        const int P0 = max(0, seq_pages(len, a.ps, a.max_pages));  // as the scoring kernel counts
+        const int P0 = P;  // as the scoring kernel counts
         // the row's page-table entries, copied while the keys are awaited (for the
         // physical page of each selected page)
         if (a.sel_phys)
@@ -327,7 +347,7 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
         if (!s_ok) return;
         unsigned* kg = a.keys + (long long)row * a.max_pages;
         const unsigned long long t0 = globaltimer_ns();
-        bool missing = gather_keys<NT>(kg, keys, P0, tid);
+        bool missing = gather_keys<NT>(kg, keys, P0, tid, note);
         while (true) {
             if (!__syncthreads_or(missing)) break;
             if (tid == 0) {
@@ -337,7 +357,7 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
             __syncthreads();
             if (!s_ok) return;
             __nanosleep(64);
-            missing = repoll_keys(kg, keys, P0, tid, NT);
+            missing = repoll_keys(kg, keys, P0, tid, NT, note);
         }
         // acquire: the fused append's writes are released before the keys of its tile
         // (the row's last), so thread 0, which publishes the row below, reads the last
@@ -358,7 +378,6 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
         __syncthreads();
         if (tid == 0) st_release(a.sel_done + row, 1u);
     };
-    const int P = max(0, seq_pages(len, a.ps, a.max_pages));  // a bad length: empty (flagged by the scoring)
     int32_t* out = a.sel + (long long)row * a.k_max;
     if (P <= 0) {
         if (tid == 0) {
@@ -368,24 +387,11 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
         publish();
         return;
     }
-    const int sink = min(a.pol.sink_pages, P), local = min(a.pol.local_pages, P);
-    const int nm = min(P, sink + local);
-    const int ncand = P - nm;
-    auto mand = [&](int p) { return p < sink || p >= P - local; };
 
-    // keys: each thread's loads are independent and issued back to back; the
-    // candidates' smallest and largest key on the way
-    if (!a.keys) __syncthreads();  // (chained: the waits above ordered the clearing)
-    uint32_t kmin = 0xffffffffu, kmax = 0u;
-    if (a.keys) {  // chained step: the keys are already in shared memory
-        for (int p = tid; p < P; p += NT) {
-            const uint32_t u = keys[p];
-            if (!mand(p)) {
-                kmin = min(kmin, u);
-                kmax = max(kmax, u);
-            }
-        }
-    } else {
+    // keys (chained step: already in shared memory, their range taken): each thread's
+    // loads are independent and issued back to back; the range on the way
+    if (!a.keys) {
+        __syncthreads();  // (chained: the waits above ordered the clearing)
         const float* sc = a.scores + (long long)row * a.max_pages;
         for (int p0 = 0; p0 < P; p0 += NT * 4) {
             float v[4];
