@@ -788,16 +788,25 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
         if constexpr (C::TRS && D == 128) {
             // Per output row one L2 round trip for the lse of every split (loaded
             // once, kept for the max, the sum and the weights), then one per batch
-            // of SB splits' o; each lane owns 4 channels.  (Issuing the first o
-            // batch with the lse saves one more round trip per row but made the
-            // page loop of this kernel measurably slower.)
-            constexpr int SB = 4;  // splits whose o loads are in flight together
+            // of SB splits' o; each lane owns 4 channels.  For pages of 32 tokens
+            // or more (whose kernels are held to one to three CTAs per SM by shared
+            // memory, not registers) eight splits at a time, the first eight issued
+            // with the lse loads; for 16-token pages four, after them (issuing them
+            // with the lse made the page loop of that kernel measurably slower).
+            constexpr bool EARLY = PS >= 32;
+            constexpr int SB = PS >= 32 ? 8 : 4;  // splits whose o loads are in flight together
             const long long rbase = (long long)cu.row * a.num_splits * R;
             const int ns = cu.nsplit;
             for (int r = mt * 16; r < min(R, mt * 16 + 16); ++r) {
                 const float* lse_r = a.part_lse + rbase + r;                // split s: lse_r[s * R]
                 const float4* o_r = reinterpret_cast<const float4*>(a.part_o + (rbase + r) * D) + lane;
                 const long long o_step = (long long)R * D / 4;              // split s: o_r[s * o_step]
+                float4 v[SB];
+                if constexpr (EARLY) {
+#pragma unroll
+                    for (int k = 0; k < SB; ++k)
+                        if (k < ns) v[k] = __ldcg(o_r + k * o_step);
+                }
                 const float ls0 = lane < ns ? __ldcg(lse_r + (long long)lane * R) : NEG_INF;
                 float M = ls0;
                 for (int s = 32 + lane; s < ns; s += 32) M = fmaxf(M, __ldcg(lse_r + (long long)s * R));
@@ -815,10 +824,11 @@ __global__ void __launch_bounds__(AttnCfg<D, PS, NMT, SPARSE, KS>::THREADS)
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (M != NEG_INF) {
                     for (int s0 = 0; s0 < ns; s0 += SB) {
-                        float4 v[SB];
+                        if (!EARLY || s0 > 0) {
 #pragma unroll
-                        for (int k = 0; k < SB; ++k)
-                            if (s0 + k < ns) v[k] = __ldcg(o_r + (s0 + k) * o_step);
+                            for (int k = 0; k < SB; ++k)
+                                if (s0 + k < ns) v[k] = __ldcg(o_r + (s0 + k) * o_step);
+                        }
 #pragma unroll
                         for (int k = 0; k < SB; ++k) {
                             const int s = s0 + k;
