@@ -444,16 +444,19 @@ def _wide_table(w, max_pages=1040):
     return w
 
 
-# name, overrides, append, variant; "chained" cases have enough rows for one
-# attention unit per row, "calls" cases run the calls one after the other
+# name, overrides, append, variant.  The step chains its kernels row by row in every
+# case; the row count (B x 8 KV heads, tiny: x 2) sets the chained selection's CTA width
+# on a 152-SM part: 128 threads above two rows per SM, 256 up to two, 512 up to one
+# (few rows: split attention units and the fused merge)
 STEP_CASES = [
-    ("q8b", dict(), True, None),                                            # full size, chained
-    ("q8b", dict(B=5, len_lo=700, len_hi=2200), True, None),                # few rows: calls in turn
-    ("q17b", dict(B=48, len_lo=2000, len_hi=6000), False, None),            # chained
-    ("longtail", dict(B=2, len_lo=4000, len_hi=9000, T=1), True, None),     # calls
+    ("q8b", dict(), True, None),                                            # full size, 512 rows
+    ("q8b", dict(B=5, len_lo=700, len_hi=2200), True, None),                # 40 rows, split units
+    ("q17b", dict(B=48, len_lo=2000, len_hi=6000), False, None),            # 384 rows
+    ("q8b", dict(B=30, len_lo=2000, len_hi=5000), True, None),              # 240 rows
+    ("longtail", dict(B=2, len_lo=4000, len_hi=9000, T=1), True, None),     # 16 rows, split units
     ("q8b", dict(B=40, len_lo=2000, len_hi=5000, page_size=32), True, None),
     ("q8b", dict(B=40, len_lo=2000, len_hi=5000, page_size=64), False, None),
-    ("tiny", dict(B=200), True, None),                                      # D = 64, chained
+    ("tiny", dict(B=200), True, None),                                      # D = 64, 400 rows
     ("q8b", dict(B=40, len_lo=2000, len_hi=5000), True, "top_p"),
     ("q8b", dict(B=40, len_lo=2000, len_hi=5000), True, "wide_table"),
 ]
@@ -519,11 +522,14 @@ def _edge_lens(n_seq, ps):
     return [pattern[i % len(pattern)] for i in range(n_seq)]
 
 
-@pytest.mark.parametrize("case", ["q17b_short", "tiny_d64", "edges_d128", "edges_d64_ps32"])
+@pytest.mark.parametrize("case", ["q17b_short", "tiny_d64", "edges_d128", "edges_d64_ps32", "rows192",
+                                  "rows64_long"])
 def test_decode_step_against_the_oracle(case):
-    """The chained decode step (no append; enough rows for one attention unit per row)
-    against the fp64 oracle: selections equal outside the tie band, outputs within
-    tolerance on the rows selected alike, empty rows give o = 0 and lse = -inf."""
+    """The chained decode step (no append) against the fp64 oracle: selections equal
+    outside the tie band, outputs within tolerance on the rows selected alike, empty
+    rows give o = 0 and lse = -inf.  The row counts cover each width of the chained
+    selection on a 152-SM part: 320 / 400 rows (128 threads), 192 rows (256) and 64 rows
+    of 750-1,250 pages (512 threads, several radix levels, split attention units)."""
     import torch
     import sparse_attention_decode_pages_gb300 as spd
     if case == "q17b_short":
@@ -531,6 +537,12 @@ def test_decode_step_against_the_oracle(case):
                      policy=wl.BudgetPolicy("fixed", fixed_pages=24, sink_pages=1, local_pages=4))
     elif case == "tiny_d64":
         w = wl.named("tiny", threads=8, B=200)
+    elif case == "rows192":
+        w = wl.named("tiny", threads=8, B=96, len_lo=3000, len_hi=8000,
+                     policy=wl.BudgetPolicy("fixed", fixed_pages=24, sink_pages=1, local_pages=4))
+    elif case == "rows64_long":
+        w = wl.named("tiny", threads=8, B=32, len_lo=12000, len_hi=20000,
+                     policy=wl.BudgetPolicy("fraction", frac_num=1, frac_den=16, sink_pages=1, local_pages=4))
     else:
         D, ps = (128, 16) if case == "edges_d128" else (64, 32)
         pol = wl.BudgetPolicy("fixed", fixed_pages=3, sink_pages=1, local_pages=1)
