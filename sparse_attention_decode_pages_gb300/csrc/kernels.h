@@ -104,6 +104,7 @@ struct ScoreSelectArgs {
     // starts when its count is complete (instead of after the whole scoring grid).
     unsigned long long* tile_ctr;  // [2]: chunk and single-tile counters, zero on entry and on exit
     unsigned* warps_done;
+    unsigned* sel_claims;          // chained step: the selection CTAs' row claims (zero on entry and on exit)
     unsigned* tiles_done;          // [B*H_kv] progress hints (NULL: not chained), zero on entry and on exit
     unsigned* sel_done;            // [B*H_kv]: set when a row's selection is written
     // [B*H_kv][max_pages] order-preserving score keys (never 0), zero on entry and

@@ -625,6 +625,7 @@ __device__ __forceinline__ void select_row_block(const ScoreSelectArgs& a, const
 template <int NT>
 __global__ void __launch_bounds__(NT) select_kernel(ScoreSelectArgs a) {
     extern __shared__ uint32_t keys[];
+    __shared__ int s_next;
     if (a.tiles_done) {
         pdl_trigger();  // each row waits for its own tiles instead of the scoring grid
     } else {
@@ -632,9 +633,27 @@ __global__ void __launch_bounds__(NT) select_kernel(ScoreSelectArgs a) {
         pdl_trigger();
     }
     const int rows = a.B * a.H_kv;
-    for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+    if (!a.sel_claims) {
+        for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+            select_row_block<NT>(a, row, keys);
+            __syncthreads();  // the shared state is reused by the next row
+        }
+        return;
+    }
+    // chained step: CTA i selects row i, then claims the next row in order as it
+    // finishes one (rows become ready in order; the CTA free first takes the next),
+    // until a claim fails.  The grid's claims total exactly `rows`: the one that
+    // returns rows - 1 is the last, and resets the counter for the next call.
+    for (int row = blockIdx.x; row < rows;) {
         select_row_block<NT>(a, row, keys);
-        __syncthreads();  // the shared state is reused by the next row
+        if (threadIdx.x == 0) {
+            const unsigned v = atomicAdd(a.sel_claims, 1u);
+            if (v == (unsigned)rows - 1u) *a.sel_claims = 0u;
+            s_next = (int)gridDim.x + (int)v;
+        }
+        __syncthreads();  // s_next, and the shared state reused by the next row
+        row = s_next;
+        __syncthreads();  // every thread has read s_next
     }
 }
 

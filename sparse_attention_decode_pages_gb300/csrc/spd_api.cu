@@ -552,7 +552,7 @@ SPD_API spd_status sparse_decode_attn(const spd_dims* dims, const spd_bf16* q, c
 }
 
 // The chained step's workspace: [score / select][chain: two tile counters, warps
-// done, tiles_done[rows], sel_done[rows], (256-aligned) keys[rows][max_pages],
+// done, selection claims, tiles_done[rows], sel_done[rows], (256-aligned) keys[rows][max_pages],
 // (256-aligned) sel_phys[rows][k_max]][attention].
 struct StepWs {
     size_t score, chain, keys, phys, attn, bytes;
@@ -629,6 +629,7 @@ SPD_API spd_status sparse_decode_step(const spd_dims* dims, spd_bf16* K, spd_bf1
     const long long rows = (long long)dims->B * dims->H_kv;
     a.tile_ctr = reinterpret_cast<unsigned long long*>(chain);
     a.warps_done = reinterpret_cast<unsigned*>(chain + 16);
+    a.sel_claims = reinterpret_cast<unsigned*>(chain + 20);
     a.tiles_done = reinterpret_cast<unsigned*>(chain + 32);
     a.sel_done = a.tiles_done + rows;
     a.keys = reinterpret_cast<unsigned*>(chain + w.keys);
