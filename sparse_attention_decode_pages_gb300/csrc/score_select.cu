@@ -633,7 +633,7 @@ __global__ void __launch_bounds__(NT) select_kernel(ScoreSelectArgs a) {
         pdl_trigger();
     }
     const int rows = a.B * a.H_kv;
-    if (!a.sel_claims) {
+    if (!a.sel_claims || (int)gridDim.x >= rows) {  // (every row its own CTA: nothing to claim)
         for (int row = blockIdx.x; row < rows; row += gridDim.x) {
             select_row_block<NT>(a, row, keys);
             __syncthreads();  // the shared state is reused by the next row
