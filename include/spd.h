@@ -283,16 +283,15 @@ spd_status sparse_decode_attn(const spd_dims *dims, const spd_bf16 *q, const spd
  * sparse_decode_attn with automatic splits).  Results -- K, V, summ, sel,
  * nsel, o, lse -- are those of the separate calls.
  *
- * When every (sequence, KV head) row is one attention unit (enough rows to
- * occupy the GPU, e.g. B = 64 at 8 KV heads), the three kernels are chained
- * row by row instead of grid by grid: scoring hands out its tiles in row order
- * and counts the finished tiles of each row, the selection of a row starts as
- * soon as its count is complete, and the attention of a row as soon as its
- * selection is published (release / acquire flags in the workspace; every
- * wait is bounded and reports SPD_DEV_TIMEOUT).  Otherwise the calls run one
- * after the other.  The workspace (spd_sparse_decode_step_workspace_size
- * bytes) must be zero before its first use and is left zero; calls that
- * overlap on the GPU need separate workspaces.  Errors as the separate calls.
+ * The three kernels are chained row by row instead of grid by grid: scoring
+ * hands out its tiles in row order and counts the finished tiles of each row,
+ * the selection of a row starts as soon as its count is complete, and the
+ * attention units of a row (one, or several and a merge when there are few
+ * rows) as soon as its selection is published (release / acquire flags in the
+ * workspace; every wait is bounded and reports SPD_DEV_TIMEOUT).  The
+ * workspace (spd_sparse_decode_step_workspace_size bytes) must be zero before
+ * its first use and is left zero; calls that overlap on the GPU need separate
+ * workspaces.  Errors as the separate calls.
  */
 size_t spd_sparse_decode_step_workspace_size(const spd_dims *dims, int32_t k_max);
 spd_status sparse_decode_step(const spd_dims *dims, spd_bf16 *K, spd_bf16 *V, const int32_t *page_table,
