@@ -457,6 +457,7 @@ STEP_CASES = [
     ("q8b", dict(B=40, len_lo=2000, len_hi=5000, page_size=32), True, None),
     ("q8b", dict(B=40, len_lo=2000, len_hi=5000, page_size=64), False, None),
     ("tiny", dict(B=200), True, None),                                      # D = 64, 400 rows
+    ("tiny", dict(B=1000), True, None),                                     # 2,000 rows: ~7 claimed per CTA
     ("q8b", dict(B=40, len_lo=2000, len_hi=5000), True, "top_p"),
     ("q8b", dict(B=40, len_lo=2000, len_hi=5000), True, "wide_table"),
 ]
